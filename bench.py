@@ -1,0 +1,423 @@
+"""Throughput of the affine group-quantized mat-vec (qmv) on one GB300.
+
+One step = one qmv call on the 12B-class decode projection (N=15360, K=3840,
+4-bit affine, group 64, bf16 scale/bias/x, fp32 accumulate, bf16 y), M = 1.
+The same measurement at M = 13 (the streamed kernel) is reported beside it.
+
+Device timing: the K steps run as CUDA-graph replays on one stream,
+bracketed by CUDA events; each step reads a different one of R copies of the
+weights whose total exceeds twice the L2 size, so weights come from HBM.
+``value`` = algorithmic bytes per call / device time per call (GB/s), the
+bytes being W + scales + biases + x + y (weights read once for all M).
+
+``e2e``: the same calls through the public Python API, each step copying x
+from pinned host memory and reading y back to pinned host memory.
+
+``--impl reference`` times the CPU oracle (fp32 factored form, all host
+cores) on the same workload instead: the oracle is the reference arm here.
+
+Launch: ``python bench.py [--gpus N --steps K --warmup W]``; for N > 1 under
+torchrun each rank runs its own replica (the path has no exchange step) and
+rank 0 prints the whole-job line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "qmv achieved HBM GB/s & % of GB300 roofline at M=1 and M=13 (µs/call)"
+WORKLOAD = "proj_15360x3840_4b_g64"
+KERNEL_SOURCES = ["qmv_kernel.cuh", "qmv_plan.h"]
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes per launch of qmv_m1 read from one ncu capture, keyed by a hash of
+# the kernel sources it was taken on (None until a capture exists).
+NCU_TRAFFIC = {}
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "group_quantized_mat_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def algorithmic_bytes(N, K, M, bits, gs):
+    return N * K * bits // 8 + 4 * N * (K // gs) + 2 * M * (K + N)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- GPU arm
+def run_gpu(args, rank, world, local_rank):
+    import torch
+
+    import group_quantized_mat_gb300 as g
+    import synth
+    from group_quantized_mat_gb300 import build as libbuild
+
+    libbuild.build()
+    g.load()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = synth.WORKLOADS[WORKLOAD]
+    N, K, bits, gs = w["N"], w["K"], w["bits"], w["group_size"]
+    inp = synth.make_inputs(N, K, 16, bits, gs, seed=0)
+    w_host = g.qmv_pack(inp.q, bits)
+
+    def tdev(a):
+        a = a.view(np.int16) if a.dtype == np.uint16 else a.view(np.int32)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    set_bytes = w_host.nbytes + inp.scales.nbytes + inp.biases.nbytes
+    R = max(2, int(np.ceil(2.0 * l2 / set_bytes)) + 1)
+    sets = [(tdev(w_host), tdev(inp.scales), tdev(inp.biases)) for _ in range(R)]
+    x_all = tdev(inp.x)
+    stream = torch.cuda.Stream(device=dev)
+    chunk = 500
+
+    def measure(M):
+        x = x_all[:M].contiguous()
+        y = torch.empty((M, N), dtype=torch.int16, device=dev)
+
+        def call(i):
+            wq, s, b = sets[i % R]
+            g.qmv_run(wq, s, b, x, y, M, N, K, bits, gs, stream=stream)
+
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                call(i)
+        torch.cuda.synchronize()
+        n_chunks, rem = divmod(args.steps, chunk)
+        graphs = []
+        with torch.cuda.stream(stream):
+            for size in ([chunk] if n_chunks else []) + ([rem] if rem else []):
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr, stream=stream):
+                    for i in range(size):
+                        call(i)
+                graphs.append(gr)
+            for gr in graphs:  # untimed replay: uploads the graphs
+                gr.replay()
+        torch.cuda.synchronize()
+        big = graphs[0] if n_chunks else None
+        tail = graphs[-1] if rem else None
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        with ClockSampler(local_rank) as clk:
+            with torch.cuda.stream(stream):
+                start.record(stream)
+                for _ in range(n_chunks):
+                    big.replay()
+                if tail is not None:
+                    tail.replay()
+                end.record(stream)
+            torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        ms = start.elapsed_time(end)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms, clk.summary()
+
+    def measure_e2e(M, steps):
+        x_host = torch.from_numpy(inp.x[:M].view(np.int16).copy()).pin_memory()
+        y_host = torch.empty((M, N), dtype=torch.int16).pin_memory()
+        x = torch.empty((M, K), dtype=torch.int16, device=dev)
+        y = torch.empty((M, N), dtype=torch.int16, device=dev)
+
+        def step(i):
+            wq, s, b = sets[i % R]
+            x.copy_(x_host, non_blocking=True)
+            g.qmv_run(wq, s, b, x, y, M, N, K, bits, gs, stream=stream)
+            y_host.copy_(y, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for i in range(min(args.warmup, 50)):
+                step(i)
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for i in range(steps):
+                step(i)
+            end.record(stream)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) / steps, M * K * 2, M * N * 2
+
+    ms1, clocks1 = measure(1)
+    ms13, clocks13 = measure(13)
+    e2e_steps = min(args.steps, 3000)
+    e2e_ms, h2d, d2h = measure_e2e(1, e2e_steps)
+    return dict(N=N, K=K, bits=bits, gs=gs, R=R, set_bytes=set_bytes, l2=l2, ms1=ms1, ms13=ms13, clocks1=clocks1,
+                clocks13=clocks13, e2e_ms=e2e_ms, e2e_steps=e2e_steps, h2d=h2d, d2h=d2h,
+                sm_count=torch.cuda.get_device_properties(dev).multi_processor_count)
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def oracle_timing(N, K, M, bits, gs, seconds=10.0, rows=None, repeats=None):
+    """fp32 factored oracle on all host cores; returns (seconds per run, threads, rows, runs)."""
+    import synth
+    from oracle import Oracle
+    o = Oracle(0)
+    inp = synth.make_inputs(N, K, M, bits, gs, seed=0)
+    rows = N if rows is None else rows
+    wq = o.pack(inp.q[:rows], bits)
+    s, b = inp.scales[:rows], inp.biases[:rows]
+    threads = len(os.sched_getaffinity(0))
+    o.qmv_f32_factored(wq, s, b, inp.x, bits, gs, nthreads=threads)  # warm
+    runs, t0 = 0, time.perf_counter()
+    used = threads
+    while True:
+        _, _, used = o.qmv_f32_factored(wq, s, b, inp.x, bits, gs, nthreads=threads)
+        runs += 1
+        el = time.perf_counter() - t0
+        if (repeats is not None and runs >= repeats) or (repeats is None and el >= seconds):
+            break
+    return el / runs, used, rows, runs
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import synth
+    w = synth.WORKLOADS[WORKLOAD]
+    N, K, bits, gs, M = w["N"], w["K"], w["bits"], w["group_size"], 1
+    t_full, threads, _, _ = oracle_timing(N, K, M, bits, gs, repeats=1)
+    budget = 60.0
+    rows = int(max(1, min(N, N * budget / max(1e-9, (args.steps + args.warmup) * t_full))))
+    if args.warmup:
+        oracle_timing(N, K, M, bits, gs, rows=rows, repeats=args.warmup)
+    t_step, threads, rows, runs = oracle_timing(N, K, M, bits, gs, rows=rows, repeats=args.steps)
+    nbytes = algorithmic_bytes(rows, K, M, bits, gs)
+    gbs = nbytes / t_step / 1e9
+    sample = f"rows 0..{rows - 1} of the {N}x{K} 4-bit g64 problem, M=1, per step; {runs} steps"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; distributions of the tiny workload)",
+        "config": {"workload": WORKLOAD, "N": N, "K": K, "M": M, "bits": bits, "group_size": gs},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return line
+
+
+def run_profile(args):
+    """Plain launches of one workload for ncu: `warmup` untimed calls, then
+    `steps` calls, each on a fresh weight copy (no graphs, no clock sampling)."""
+    import torch
+
+    import group_quantized_mat_gb300 as g
+    import synth
+    from group_quantized_mat_gb300 import build as libbuild
+
+    libbuild.build()
+    g.load()
+    w = synth.WORKLOADS[args.workload]
+    N, K, bits, gs, M = w["N"], w["K"], w["bits"], w["group_size"], args.M
+    inp = synth.make_inputs(N, K, M, bits, gs, seed=0)
+    wq = g.qmv_pack(inp.q, bits)
+
+    def tdev(a):
+        a = a.view(np.int16) if a.dtype == np.uint16 else a.view(np.int32)
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    copies = 2
+    sets = [(tdev(wq), tdev(inp.scales), tdev(inp.biases)) for _ in range(copies)]
+    x = tdev(inp.x)
+    y = torch.empty((M, N), dtype=torch.int16, device="cuda")
+    for i in range(args.warmup + args.steps):
+        wd, sd, bd = sets[i % copies]
+        g.qmv_run(wd, sd, bd, x, y, M, N, K, bits, gs)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": args.workload, "M": M, "launches": args.warmup + args.steps,
+                      "bytes_per_launch": algorithmic_bytes(N, K, M, bits, gs)}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--profile", action="store_true", help="plain launches for ncu (see run_profile)")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--M", type=int, default=1)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.profile:
+        run_profile(args)
+        return
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    r = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        N, K, bits, gs = r["N"], r["K"], r["bits"], r["gs"]
+        b1 = algorithmic_bytes(N, K, 1, bits, gs)
+        b13 = algorithmic_bytes(N, K, 13, bits, gs)
+        us1 = r["ms1"] * 1e3 / args.steps
+        us13 = r["ms13"] * 1e3 / args.steps
+        gbs1 = b1 / (us1 * 1e-6) / 1e9
+        gbs13 = b13 / (us13 * 1e-6) / 1e9
+        peak, peak_kind = measured_peaks()
+        cpu_t, cpu_threads, cpu_rows, cpu_runs = oracle_timing(N, K, 1, bits, gs, seconds=args.cpu_seconds)
+        cpu_gbs = b1 / cpu_t / 1e9
+        e2e_gbs = b1 / (r["e2e_ms"] * 1e-3) / 1e9
+        kh = kernel_hash()
+        traffic = NCU_TRAFFIC.get(kh)
+        # FP32-lane roofline for the streamed case: 2 flop per (element, vector)
+        fma_peak_tflops = r["sm_count"] * 128 * 2 * 2.07e9 / 1e12
+        flops13 = 2.0 * N * K * 13
+        line = {
+            "metric": METRIC,
+            "value": round(world * gbs1, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(r["ms1"] / args.steps, 6),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic (seeded: q~U{0..15}, scale~U(0.001,0.02) bf16, bias=-8*scale+N(0,1e-3) bf16, x~N(0,1) bf16)",
+            "config": {"workload": WORKLOAD, "N": N, "K": K, "M": 1, "bits": bits, "group_size": gs,
+                       "l2": f"inputs > L2: {r['R']} rotating weight copies of {r['set_bytes'] / 1e6:.1f} MB "
+                             f"({r['R'] * r['set_bytes'] / 1e6:.0f} MB) vs L2 {r['l2'] / 1e6:.0f} MB",
+                       "timing": "CUDA-graph replays of 500 calls, CUDA events on the launch stream",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "us_per_call": round(us1, 3),
+            "roofline": {"bound": "hbm", "achieved": round(gbs1, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs1 / peak, 4), "traffic": traffic,
+                         "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                         if peak_kind == "measured" else "fallback 6.8 TB/s",
+                         "kernel": "qmv_m1<4,64>", "bytes_per_launch": b1},
+            "m13": {"us_per_call": round(us13, 3), "achieved_gbs": round(gbs13, 2),
+                    "hbm_frac": round(gbs13 / peak, 4), "ratio_to_m1": round(us13 / us1, 3),
+                    "fp32_tflops": round(flops13 / (us13 * 1e-6) / 1e12, 2),
+                    "fp32_lane_peak_tflops": round(fma_peak_tflops, 1),
+                    "fp32_frac": round(flops13 / (us13 * 1e-6) / 1e12 / fma_peak_tflops, 4),
+                    "kernel": "qmv_streamed<4,64,13>", "bytes_per_launch": b13, "clocks": r["clocks13"]},
+            "clocks": r["clocks1"],
+            "e2e": {"value": round(world * e2e_gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
+                    "d2h_bytes_per_step": r["d2h"], "us_per_step": round(r["e2e_ms"] * 1e3, 3),
+                    "steps": r["e2e_steps"], "api": "group_quantized_mat_gb300.qmv_run (C ABI qmv_run)"},
+            "gpu_launches": args.steps,
+            "cpu_baseline": {"value": round(cpu_gbs, 4), "unit": "GB/s", "cores": cpu_threads, "kind": "oracle",
+                             "sample": f"full {N}x{K} M=1 problem (fp32 factored oracle), {cpu_runs} runs"},
+            "kernel_hash": kh,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,10 @@
+// Kernels for bits = 4, group_size = 64.
+#include "qmv_launch.cuh"
+
+namespace qmv {
+cudaError_t launch_b4g64(int V, const CUtensorMap &map, const Params &p, int grid_y, size_t smem,
+                           cudaStream_t stream)
+{
+    return launch_bits_gs<4, 64>(V, map, p, grid_y, smem, stream);
+}
+}  // namespace qmv

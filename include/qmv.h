@@ -1,0 +1,180 @@
+/*
+ * qmv.h -- C ABI of the GB300 (sm_103a) affine group-quantized mat-vec library.
+ *
+ *   y[m, n] = sum_i ( s[n, i/gs] * q[n, i] + b[n, i/gs] ) * x[m, i]
+ *
+ * for M activation vectors x[M, K] (bf16), N output rows, packed b-bit weights
+ * q (bits = 4 or 2), one bf16 scale s and one bf16 bias b per group of gs = 64
+ * or 128 consecutive weights along K, bf16 output y[M, N].
+ *
+ * Source of the operation (group_quantized_mat pages):
+ *  - mlxcel issue #1289 "perf(metal): an order-preserving streamed qmv ...":
+ *    section "Correction to the obvious sketch: qdot does not dequantize"
+ *    (the affine form scale*q + bias, the factored group dot
+ *    scale*sum(q*x) + bias*sum(x), the field masks of a packed word);
+ *    sections "The observation this rests on" and "Step 2" (one weight read
+ *    serving M streamed vectors, each result bit-identical to the M = 1 run).
+ *  - llama.cpp PR #159 "metal: PQ2_0 and Q2_0 mat-vec dot in exact float",
+ *    section "How" (2-bit fields, field 0 in the low bits; group sizes 64
+ *    and 128).
+ *  - mlxcel PR #1681 "perf(cuda/quant): block output rows per warp ...",
+ *    section "Not covered" (scale and bias applied once per group).
+ *
+ * Every function here is host code. Pointers documented as "device" must be
+ * device (or managed) memory of the current CUDA device; "host" pointers are
+ * ordinary host memory. The library never takes ownership of a caller's
+ * buffer and never frees one.
+ */
+#ifndef QMV_H
+#define QMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Symbols of the shared library (it is built with hidden default visibility). */
+#if defined(__GNUC__)
+#define QMV_API __attribute__((visibility("default")))
+#else
+#define QMV_API
+#endif
+
+/* Return codes. Every entry point validates its arguments on the host before
+ * touching the GPU and returns a code instead of launching on bad input. */
+typedef enum qmv_status {
+    QMV_OK = 0,
+    QMV_ERR_NULL = 1,       /* a required pointer is NULL                                  */
+    QMV_ERR_BITS = 2,       /* bits is not 2 or 4                                          */
+    QMV_ERR_GROUP = 3,      /* group_size is not 64 or 128                                 */
+    QMV_ERR_SHAPE = 4,      /* N < 1, K < 1, K % group_size != 0, or a size overflows      */
+    QMV_ERR_M_RANGE = 5,    /* M is not in [1, QMV_MAX_M]                                  */
+    QMV_ERR_ALIGN = 6,      /* w_q, x or workspace not 16-byte aligned; scales, biases or y
+                               not 2-byte aligned (4 for an fp32 y)                       */
+    QMV_ERR_CUDA = 7,       /* a CUDA runtime call failed (launch, device query, encode)   */
+    QMV_ERR_WORKSPACE = 8,  /* workspace is smaller than qmv_workspace_size()              */
+    QMV_ERR_VALUE = 9,      /* qmv_pack: an input value does not fit in `bits` bits        */
+    QMV_ERR_FLAGS = 10      /* unknown bits set in `flags`                                 */
+} qmv_status;
+
+/* The CUDA stream type (identical to cudaStream_t; 0 is the legacy default stream). */
+typedef struct CUstream_st *qmv_stream_t;
+
+/* Widest activation batch one call serves from a single read of the weights
+ * (the speculative-verify width; above it a dense quantized mat-mat takes over,
+ * issue #1289 "Scope limits"). */
+#define QMV_MAX_M 16
+
+/* ------------------------------------------------------------------ codec */
+
+/* Number of uint32 words of the packed weight matrix: N * K * bits / 32.
+ * Returns 0 for invalid arguments (bits not in {2,4}, N < 1, K < 1, or K * bits
+ * not a multiple of 32). */
+QMV_API size_t qmv_packed_words(int64_t N, int64_t K, int bits);
+
+/* Packs q[N, K] (host, row-major uint8, each value < 2^bits) into
+ * w_q[N, K*bits/32] (host, row-major uint32, caller-allocated). Field j of a
+ * word holds element (word_index * 32/bits + j) of the row at bit positions
+ * [bits*j, bits*j + bits): field 0 in the low bits, little-endian
+ * (issue #1289 "Correction..."; PR #159 "How").
+ * Errors: QMV_ERR_NULL, QMV_ERR_BITS, QMV_ERR_SHAPE (K*bits % 32 != 0),
+ * QMV_ERR_VALUE (a value >= 2^bits; w_q is then left unspecified). */
+QMV_API qmv_status qmv_pack(const uint8_t *q, uint32_t *w_q, int64_t N, int64_t K, int bits);
+
+/* Inverse of qmv_pack (host to host). Same errors except QMV_ERR_VALUE. */
+QMV_API qmv_status qmv_unpack(const uint32_t *w_q, uint8_t *q, int64_t N, int64_t K, int bits);
+
+/* ------------------------------------------------------------------- plan */
+
+/* Number of contiguous K-splits the kernels use for a (N, K, bits, group_size)
+ * problem, or 0 for invalid arguments. It depends on K, bits and group_size
+ * only -- never on M -- so the fp32 summation order of every output is the
+ * same for every M (the basis of the bit-identity guarantee below). */
+QMV_API int qmv_split_count(int N, int K, int bits, int group_size);
+
+/* Bytes of device workspace a call with these arguments needs (0 when the
+ * problem has a single K-split). Returns 0 for invalid arguments too. */
+QMV_API size_t qmv_workspace_size(int M, int N, int K, int bits, int group_size);
+
+/* ------------------------------------------------------------------- run */
+
+/* y = W . x for M vectors, asynchronously on `stream`.
+ *
+ *  w_q     device, uint32 [N, K*bits/32] from qmv_pack, 16-byte aligned.
+ *  scales  device, bf16 bit patterns [N, K/group_size], row-major, 2-byte aligned.
+ *  biases  device, bf16 bit patterns [N, K/group_size], row-major, 2-byte aligned.
+ *  x       device, bf16 [M, K], row-major (vector-major), 16-byte aligned.
+ *  y       device, bf16 [M, N], row-major; must not overlap any input.
+ *  M       1 .. QMV_MAX_M.  N, K >= 1; K a multiple of group_size.
+ *  bits    4 or 2.  group_size 64 or 128.
+ *
+ * Arithmetic: fp32. Each group is evaluated in the factored form
+ * s * (sum q x) + b * (sum x) (no dequantized weight is formed), then rounded
+ * once to bf16 (nearest even). The fp32 operation order for an output element
+ * depends only on (N, K, bits, group_size) and the element's row: column j of
+ * an M-vector call is bit-identical to an M = 1 call on x[j] (issue #1289
+ * "The observation this rests on": "bit-identical ... by construction").
+ *
+ * The call returns after enqueueing; it never synchronizes. A problem with
+ * more than one K-split needs scratch: qmv_run uses a workspace owned by the
+ * library, one per device, allocated (cudaMalloc) on the first call that needs
+ * more than the current one and kept until exit. That first call is not
+ * stream-ordered and must not be made during stream capture; calls that share
+ * the library workspace must not overlap on the GPU (use qmv_run_ex with
+ * separate workspaces for concurrent streams).
+ *
+ * Errors: QMV_ERR_NULL, QMV_ERR_BITS, QMV_ERR_GROUP, QMV_ERR_SHAPE,
+ * QMV_ERR_M_RANGE, QMV_ERR_ALIGN (host checks, nothing launched);
+ * QMV_ERR_CUDA when the workspace allocation, the tensor-map encode or the
+ * launch fails (cudaGetLastError is consumed). */
+QMV_API qmv_status qmv_run(const uint32_t *w_q, const uint16_t *scales, const uint16_t *biases,
+                   const uint16_t *x, uint16_t *y, int M, int N, int K, int bits,
+                   int group_size, qmv_stream_t stream);
+
+/* Flags for qmv_run_ex. */
+#define QMV_F32_OUT 0x1u             /* y is float [M, N]: the fp32 value before bf16 rounding */
+#define QMV_FORCE_M1_PER_COLUMN 0x2u /* serve the M vectors as M separate M = 1 launches       */
+
+/* qmv_run with an explicit workspace and flags.
+ *
+ *  workspace        device, 16-byte aligned, at least qmv_workspace_size(M, N, K,
+ *                   bits, group_size) bytes, or NULL to use the library workspace.
+ *                   It must be all zero before its first use (qmv_workspace_init
+ *                   or cudaMemset); every completed call leaves it all zero again,
+ *                   so one workspace serves any sequence of problem shapes. Calls
+ *                   sharing one workspace must not overlap on the GPU. After a
+ *                   device error (qmv_device_error) zero it again.
+ *  workspace_bytes  its size in bytes (ignored when workspace is NULL).
+ *  flags            bitwise OR of QMV_* flags above.
+ * Additional errors: QMV_ERR_WORKSPACE, QMV_ERR_FLAGS. */
+QMV_API qmv_status qmv_run_ex(const uint32_t *w_q, const uint16_t *scales, const uint16_t *biases,
+                      const uint16_t *x, void *y, int M, int N, int K, int bits,
+                      int group_size, void *workspace, size_t workspace_bytes,
+                      unsigned flags, qmv_stream_t stream);
+
+/* Zero-fills `bytes` of a caller workspace on `stream` (cudaMemsetAsync). */
+QMV_API qmv_status qmv_workspace_init(void *workspace, size_t bytes, qmv_stream_t stream);
+
+/* ------------------------------------------------------------ diagnostics */
+
+/* Device-side error word of the current device: kernels set bit 0 when a
+ * bounded wait for a weight tile ran out (the output of that launch is then
+ * invalid). Synchronizes the device, stores the word in *word and clears it.
+ * Errors: QMV_ERR_NULL, QMV_ERR_CUDA. */
+QMV_API qmv_status qmv_device_error(unsigned *word);
+
+/* Description of the last CUDA failure behind a QMV_ERR_CUDA returned to the
+ * calling thread (the failing call, the CUDA error name and text). The string
+ * is owned by the library and valid until the thread's next failing call. */
+QMV_API const char *qmv_last_cuda_error(void);
+
+/* Static, human-readable name of a status code. Never NULL. */
+QMV_API const char *qmv_status_string(qmv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMV_H */

@@ -1,0 +1,138 @@
+"""Host-side checks of the C-ABI library (no GPU needed): it loads, it exports
+every symbol the header declares, the codec matches the oracle's packing bit
+for bit, and argument validation rejects bad calls before touching a GPU."""
+
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import group_quantized_mat_gb300 as g
+import synth
+from oracle import Oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qmv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from group_quantized_mat_gb300 import build
+    build.build()
+    return g.load()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"QMV_API\s+[\w\s\*]+?\b(qmv_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = header_functions()
+    assert set(names) == set(g.EXPORTED), names
+
+
+def test_library_exports_every_header_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", g.LIB_PATH], capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    missing = [n for n in header_functions() if n not in exported]
+    assert not missing, missing
+    for n in header_functions():
+        assert hasattr(lib, n)
+
+
+def test_library_has_no_torch_dependency(lib):
+    out = subprocess.run(["ldd", g.LIB_PATH], capture_output=True, text=True).stdout
+    assert "torch" not in out and "libcudart.so" not in out
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_pack_matches_oracle_and_roundtrips(lib, bits):
+    o = Oracle(0)
+    for N, K, seed in [(3, 64, 1), (17, 384, 2), (64, 1024, 3)]:
+        inp = synth.make_inputs(N, K, 1, bits, 64, seed)
+        ours = g.qmv_pack(inp.q, bits)
+        ref = o.pack(inp.q, bits)
+        assert ours.dtype == np.uint32 and np.array_equal(ours, ref)
+        assert np.array_equal(g.qmv_unpack(ours, K, bits), inp.q)
+        assert g.qmv_packed_words(N, K, bits) == ours.size
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_pack_every_byte_value(lib, bits):
+    """All 256 byte values through the library codec against the oracle's
+    shift/mask fields and the float-floor chain (llama.cpp PR #159, "How")."""
+    o = Oracle(0)
+    per_byte = 8 // bits
+    fields = np.array([o.byte_fields(b, bits) for b in range(256)], dtype=np.uint8)  # [256, per_byte]
+    ff = np.array([o.byte_fields_floatfloor(b, bits) for b in range(256)], dtype=np.uint8)
+    assert np.array_equal(fields, ff)
+    q = fields.reshape(1, 256 * per_byte)
+    w = g.qmv_pack(q, bits)
+    assert np.array_equal(w.view(np.uint8).ravel(), np.arange(256, dtype=np.uint8))
+    assert np.array_equal(g.qmv_unpack(w, 256 * per_byte, bits), q)
+
+
+def test_pack_rejects_bad_input(lib):
+    with pytest.raises(g.QmvError) as e:
+        g.qmv_pack(np.full((2, 64), 16, np.uint8), 4)
+    assert e.value.code == 9
+    with pytest.raises(g.QmvError) as e:
+        g.qmv_pack(np.zeros((2, 64), np.uint8), 3)
+    assert e.value.code == 2
+    with pytest.raises(g.QmvError) as e:
+        g.qmv_pack(np.zeros((2, 12), np.uint8), 4)
+    assert e.value.code == 4
+    assert lib.qmv_pack(None, None, 1, 64, 4) == 1
+    assert g.qmv_packed_words(1, 12, 4) == 0
+
+
+def test_split_plan(lib):
+    # the K-split count is a function of K, bits and group size only
+    assert g.qmv_split_count(15360, 3840, 4, 64) == g.qmv_split_count(7, 3840, 4, 64) == 3
+    assert g.qmv_split_count(256, 1024, 4, 64) == 1
+    assert g.qmv_split_count(3840, 15360, 4, 64) == 10
+    assert g.qmv_split_count(1, 1000, 4, 64) == 0
+    assert g.qmv_workspace_size(1, 256, 1024, 4, 64) == 0
+    # M = 1: x of all of K fits in one CTA's shared memory, so one CTA folds
+    # every chunk of a row tile itself and no workspace is needed
+    assert g.qmv_workspace_size(1, 15360, 3840, 4, 64) == 0
+    # M = 13: one chunk per CTA; chunk values meet in the workspace
+    w13 = g.qmv_workspace_size(13, 15360, 3840, 4, 64)
+    assert w13 == 1024 + 3 * 13 * 15360 * 4
+    assert g.qmv_workspace_size(16, 15360, 3840, 4, 64) == 1024 + 3 * 16 * 15360 * 4
+    assert g.qmv_workspace_size(17, 15360, 3840, 4, 64) == 0
+
+
+FAKE = 1 << 20  # an aligned address that validation must reject before any use
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(w_q=0), 1), (dict(y=0), 1),
+    (dict(bits=3), 2), (dict(group_size=32), 3),
+    (dict(K=1000), 4), (dict(N=0), 4), (dict(K=0), 4),
+    (dict(M=0), 5), (dict(M=17), 5),
+    (dict(w_q=FAKE + 8), 6), (dict(x=FAKE + 2), 6), (dict(scales=FAKE + 1), 6),
+])
+def test_run_validation_before_gpu(lib, kw, code):
+    args = dict(w_q=FAKE, scales=FAKE, biases=FAKE, x=FAKE, y=FAKE, M=1, N=64, K=1024, bits=4, group_size=64)
+    args.update(kw)
+    r = lib.qmv_run(args["w_q"] or None, args["scales"], args["biases"], args["x"], args["y"] or None,
+                    args["M"], args["N"], args["K"], args["bits"], args["group_size"], None)
+    assert r == code, g.qmv_status_string(r)
+
+
+def test_run_ex_rejects_flags(lib):
+    r = lib.qmv_run_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 64, 1024, 4, 64, None, 0, 0x100, None)
+    assert r == 10
+    r = lib.qmv_run_ex(FAKE, FAKE, FAKE, FAKE, FAKE + 2, 1, 64, 1024, 4, 64, None, 0, g.F32_OUT, None)
+    assert r == 6
+
+
+def test_status_strings(lib):
+    for code in range(11):
+        s = g.qmv_status_string(code)
+        assert s.startswith(g.STATUS[code])
+    assert "unknown" in g.qmv_status_string(99)

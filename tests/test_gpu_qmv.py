@@ -1,0 +1,205 @@
+"""GPU tests through the C ABI: parity with the CPU oracle and bitwise
+identity of the streamed kernel's columns with the M = 1 kernel.
+
+Acceptance (per output element): |y_gpu - y_oracle| <= 8e-3 * sum_i |w_i x_i| + 1e-5,
+y_oracle the fp64 dequantize-then-dot form. Streamed columns must equal the
+M = 1 result bit for bit (mlxcel issue #1289, "The observation this rests on":
+"bit-identical to qmv at M = 1 by construction, not by tolerance").
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import group_quantized_mat_gb300 as g
+import synth
+from gpu_helpers import DeviceProblem, check_parity, dev, oracle_rows
+from oracle import Oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from group_quantized_mat_gb300 import build
+    build.build()
+    g.load()
+    yield
+    assert g.qmv_device_error() == 0, "a kernel reported a timed-out wait"
+
+
+@pytest.fixture(scope="module")
+def o():
+    return Oracle(0)
+
+
+# ----------------------------------------------------------- full parity --
+# Sizes the oracle finishes in seconds that span several row tiles, several
+# K-splits and ragged tails (N not a multiple of 64 or 8; partial last stage).
+MEDIUM = [
+    (256, 1024, 1, 4, 64),      # the tiny workload
+    (200, 3840, 3, 4, 64),      # K of the 12B projection: 3 splits, 7.5 stages each side
+    (130, 15360, 2, 4, 64),     # K of the down projection: 10 splits
+    (77, 5120, 16, 4, 64),      # widest M
+    (300, 3840, 13, 2, 64),
+    (150, 3840, 5, 2, 128),
+    (129, 2048, 4, 4, 128),
+    (9, 384, 1, 4, 128),        # one partial box per row
+    (1, 64, 1, 4, 64),          # a single group and a single row
+    (65, 128, 7, 2, 128),
+    (64, 17408, 2, 4, 64),      # 17 splits
+]
+
+
+@pytest.mark.parametrize("N,K,M,bits,gs", MEDIUM)
+def test_parity_full_output(o, N, K, M, bits, gs):
+    inp = synth.make_inputs(N, K, M, bits, gs, seed=N + K + M)
+    dp = DeviceProblem(inp)
+    y = dp.run()
+    ref, terms = oracle_rows(o, inp)
+    check_parity(y, ref, terms, f"{(N, K, M, bits, gs)}")
+    # the fp32 value before rounding is far closer than the bf16 tolerance
+    y32 = dp.run(flags=g.F32_OUT)
+    assert np.all(np.abs(y32 - ref) <= 1e-4 * terms + 1e-6)
+    # and the bf16 output is its round-to-nearest-even
+    rne = torch.from_numpy(y32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(rne, y)
+
+
+# ------------------------------------------------- full sizes, sampled --
+FULL = [
+    ("proj_15360x3840_4b_g64", 1), ("proj_15360x3840_4b_g64", 13),
+    ("down_3840x15360_4b_g64", 1), ("down_3840x15360_4b_g64", 16),
+    ("l27b_5120x5120_4b_g64", 13), ("l27b_1024x5120_4b_g64", 1),
+    ("l27b_17408x5120_4b_g64", 1), ("l27b_5120x17408_4b_g64", 13),
+    ("proj_15360x3840_2b_g64", 13), ("proj_15360x3840_2b_g128", 1),
+]
+
+
+@pytest.mark.parametrize("name,M", FULL)
+def test_parity_full_size_sampled_rows(o, name, M):
+    w = synth.WORKLOADS[name]
+    inp = synth.make_inputs(w["N"], w["K"], M, w["bits"], w["group_size"], seed=0)
+    y = DeviceProblem(inp).run()
+    rng = np.random.default_rng(M)
+    N = w["N"]
+    rows = np.unique(np.concatenate([rng.choice(N, 96, replace=False), [0, 1, 63, 64, N - 65, N - 1]]))
+    ref, terms = oracle_rows(o, inp, rows)
+    check_parity(y[:, rows], ref, terms, f"{name} M={M}")
+
+
+# ------------------------------------------------------- bit identity --
+IDENT = [
+    (15360, 3840, 4, 64), (3840, 15360, 4, 64), (1000, 5120, 4, 64),
+    (15360, 3840, 2, 64), (15360, 3840, 2, 128), (333, 1024, 4, 128),
+]
+
+
+@pytest.mark.parametrize("N,K,bits,gs", IDENT)
+def test_streamed_columns_bit_identical_to_m1(N, K, bits, gs):
+    inp = synth.make_inputs(N, K, 16, bits, gs, seed=7)
+    dp = DeviceProblem(inp)
+    singles_bf = np.stack([dp.run(x=dp.x[m:m + 1].contiguous(), M=1)[0] for m in range(16)])
+    singles_32 = np.stack([dp.run(x=dp.x[m:m + 1].contiguous(), M=1, flags=g.F32_OUT)[0] for m in range(16)])
+    for M in (2, 4, 5, 10, 13, 16):
+        x = dp.x[:M].contiguous()
+        y_bf = dp.run(x=x, M=M)
+        y_32 = dp.run(x=x, M=M, flags=g.F32_OUT)
+        assert np.array_equal(y_bf, singles_bf[:M]), f"M={M}: bf16 columns differ from M=1"
+        assert np.array_equal(y_32.view(np.uint32), singles_32[:M].view(np.uint32)), f"M={M}: fp32 columns differ"
+        per_col = dp.run(x=x, M=M, flags=g.F32_OUT | g.FORCE_M1_PER_COLUMN)
+        assert np.array_equal(per_col.view(np.uint32), y_32.view(np.uint32))
+
+
+def test_position_invariance():
+    inp = synth.make_inputs(3840, 3840, 13, 4, 64, seed=11)
+    dp = DeviceProblem(inp)
+    x = dp.x
+    perm = list(range(1, 13)) + [0]          # vector 0 moves to the last column
+    ya = dp.run(x=x, M=13, flags=g.F32_OUT)
+    yb = dp.run(x=x[perm].contiguous(), M=13, flags=g.F32_OUT)
+    assert np.array_equal(ya[0].view(np.uint32), yb[12].view(np.uint32))
+    assert np.array_equal(ya[perm].view(np.uint32), yb.view(np.uint32))
+
+
+def test_mutated_order_is_detected(o, tmp_path):
+    """A build whose streamed kernel folds in a different order still passes
+    the tolerance, and the bit-identity check must reject it."""
+    from group_quantized_mat_gb300 import build
+    path = build.build(extra_defines=("QMV_TEST_MUTATE_ORDER=1",),
+                       out=str(build.LIB).replace("libqmv.so", "libqmv_mutant.so"))
+    mut = g.load(path)
+    inp = synth.make_inputs(512, 3840, 4, 4, 64, seed=3)
+    dp = DeviceProblem(inp)
+    y4 = dp.run(M=4, flags=g.F32_OUT, lib=mut)
+    singles = np.stack([dp.run(x=dp.x[m:m + 1].contiguous(), M=1, flags=g.F32_OUT, lib=mut)[0] for m in range(4)])
+    ref, terms = oracle_rows(o, inp)
+    assert np.all(np.abs(y4 - ref) <= 1e-4 * terms + 1e-6)
+    assert not np.array_equal(y4.view(np.uint32), singles.view(np.uint32))
+
+
+# ----------------------------------------------------------- workspace --
+def test_explicit_workspace_matches_library_workspace():
+    inp = synth.make_inputs(1000, 3840, 13, 4, 64, seed=5)
+    dp = DeviceProblem(inp)
+    y_lib = dp.run(flags=g.F32_OUT)
+    nbytes = g.qmv_workspace_size(13, 1000, 3840, 4, 64)
+    ws = torch.empty(nbytes // 4 + 4, dtype=torch.int32, device="cuda")
+    g.qmv_workspace_init(ws, nbytes)
+    for _ in range(3):  # the counters return to zero after every call
+        y = dp.run(flags=g.F32_OUT, workspace=ws, workspace_bytes=nbytes)
+        assert np.array_equal(y.view(np.uint32), y_lib.view(np.uint32))
+    with pytest.raises(g.QmvError) as e:
+        dp.run(flags=g.F32_OUT, workspace=ws, workspace_bytes=nbytes - 4)
+    assert e.value.code == 8
+
+
+def test_streams_and_back_to_back_calls():
+    """Different problems alternating on one stream share the library workspace."""
+    a = DeviceProblem(synth.make_inputs(640, 15360, 3, 4, 64, seed=1))
+    b = DeviceProblem(synth.make_inputs(700, 3840, 9, 4, 64, seed=2))
+    ya, yb = a.run(), b.run()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            assert np.array_equal(a.run(), ya)
+            assert np.array_equal(b.run(), yb)
+
+
+def test_cuda_graph_capture_replays_identically():
+    dp = DeviceProblem(synth.make_inputs(2048, 3840, 5, 4, 64, seed=4))
+    y_ref = dp.run()  # first call sizes the library workspace outside capture
+    y = torch.empty((5, 2048), dtype=torch.int16, device="cuda")
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            g.qmv_run(dp.w, dp.s, dp.b, dp.x, y, 5, 2048, 3840, 4, 64, stream=s)
+    for _ in range(3):
+        y.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(y.cpu().numpy().view(np.uint16), y_ref)
+
+
+def test_workspace_serves_any_shape_sequence():
+    """One workspace, problems of different N / K / M in turn: every call must
+    match a fresh-workspace result, and the workspace must be zero afterwards."""
+    probs = [DeviceProblem(synth.make_inputs(3840, 15360, 16, 4, 64, seed=21)),
+             DeviceProblem(synth.make_inputs(5120, 5120, 13, 4, 64, seed=22)),
+             DeviceProblem(synth.make_inputs(1000, 3840, 3, 2, 128, seed=23))]
+    need = max(g.qmv_workspace_size(p.M, p.N, p.K, p.bits, p.gs) for p in probs)
+    refs = []
+    for p in probs:
+        nb = g.qmv_workspace_size(p.M, p.N, p.K, p.bits, p.gs)
+        fresh = torch.zeros(nb // 4 + 4, dtype=torch.int32, device="cuda")
+        refs.append(p.run(flags=g.F32_OUT, workspace=fresh, workspace_bytes=nb))
+    ws = torch.zeros(need // 4 + 4, dtype=torch.int32, device="cuda")
+    for rnd in range(2):
+        for p, ref in zip(probs, refs):
+            y = p.run(flags=g.F32_OUT, workspace=ws, workspace_bytes=need)
+            assert np.array_equal(y.view(np.uint32), ref.view(np.uint32)), f"round {rnd} N={p.N}"
+    torch.cuda.synchronize()
+    assert int(torch.count_nonzero(ws)) == 0
