@@ -32,7 +32,7 @@ STATUS = {
 }
 
 EXPORTED = ("qmv_packed_words", "qmv_pack", "qmv_unpack", "qmv_split_count", "qmv_workspace_size",
-            "qmv_run", "qmv_run_ex", "qmv_workspace_init", "qmv_device_error", "qmv_last_cuda_error",
+            "qmv_run", "qmv_run_ex", "qmv_run_noalloc", "qmv_workspace_init", "qmv_device_error", "qmv_last_cuda_error",
             "qmv_status_string")
 
 
@@ -74,6 +74,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.qmv_run.argtypes = [P, P, P, P, P, I, I, I, I, I, P]
         lib.qmv_run_ex.restype = I
         lib.qmv_run_ex.argtypes = [P, P, P, P, P, I, I, I, I, I, P, SZ, U, P]
+        lib.qmv_run_noalloc.restype = I
+        lib.qmv_run_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, P]
         lib.qmv_workspace_init.restype = I
         lib.qmv_workspace_init.argtypes = [P, SZ, P]
         lib.qmv_device_error.restype = I
@@ -164,6 +166,17 @@ def qmv_run_ex(w_q, scales, biases, x, y, M: int, N: int, K: int, bits: int, gro
     code = load().qmv_run_ex(_ptr(w_q), _ptr(scales), _ptr(biases), _ptr(x), _ptr(y), M, N, K, bits, group_size,
                              _ptr(workspace), int(workspace_bytes), int(flags), _stream(stream))
     _check(code, "qmv_run_ex")
+
+
+NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def qmv_run_noalloc(w_q, scales, biases, x, y, M: int, N: int, K: int, bits: int, group_size: int,
+                    stream=None) -> None:
+    """qmv_run without any device allocation (fixed scratch array in the library)."""
+    code = load().qmv_run_noalloc(_ptr(w_q), _ptr(scales), _ptr(biases), _ptr(x), _ptr(y), M, N, K, bits,
+                                  group_size, _stream(stream))
+    _check(code, "qmv_run_noalloc")
 
 
 def qmv_workspace_init(workspace, nbytes: int, stream=None) -> None:

@@ -154,6 +154,37 @@ QMV_API qmv_status qmv_run_ex(const uint32_t *w_q, const uint16_t *scales, const
                       int group_size, void *workspace, size_t workspace_bytes,
                       unsigned flags, qmv_stream_t stream);
 
+/* Size of the fixed scratch array behind qmv_run_noalloc (4 MiB per device). */
+#define QMV_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* qmv_run without any device allocation. The paper has no counterpart: this
+ * entry point exists for callers that cannot call cudaMalloc -- code running
+ * during CUDA graph capture (an allocation is not stream-ordered and breaks
+ * or serializes the capture), engines whose device memory all belongs to
+ * their own pool allocator, and latency-bound decode loops where cudaMalloc's
+ * implicit device synchronization is not acceptable. qmv_run allocates its
+ * workspace on first use and qmv_run_ex needs a caller-allocated one; this
+ * call needs neither.
+ *
+ * Arguments, layouts, results (bit for bit) and the host-side errors are those
+ * of qmv_run. The scratch that K-split problems need comes from one static
+ * device array of QMV_NOALLOC_SCRATCH_BYTES that every GPU loading the library
+ * holds until exit; no cudaMalloc, cudaFree or allocating library routine is
+ * called. Each call clears the part of it that must start at zero
+ * (cudaMemsetAsync on `stream`). All calls on a device share the array, so
+ * calls that overlap on the GPU (other streams, or concurrent host threads)
+ * race and give undefined results.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.
+ *
+ * Errors: as qmv_run, plus QMV_ERR_WORKSPACE when the problem's
+ * qmv_workspace_size() exceeds QMV_NOALLOC_SCRATCH_BYTES (nothing launched). */
+QMV_API qmv_status qmv_run_noalloc(const uint32_t *w_q, const uint16_t *scales, const uint16_t *biases,
+                                   const uint16_t *x, uint16_t *y, int M, int N, int K, int bits,
+                                   int group_size, qmv_stream_t stream);
+
 /* Zero-fills `bytes` of a caller workspace on `stream` (cudaMemsetAsync). */
 QMV_API qmv_status qmv_workspace_init(void *workspace, size_t bytes, qmv_stream_t stream);
 
