@@ -2,9 +2,9 @@
 #include "qmv_launch.cuh"
 
 namespace qmv {
-cudaError_t launch_b4g64(int V, const CUtensorMap &map, const Params &p, int grid_y, size_t smem,
-                           cudaStream_t stream)
+cudaError_t launch_b4g64(int V, int R, const CUtensorMap &map, const Params &p, dim3 grid, int threads,
+                          size_t smem, cudaStream_t stream)
 {
-    return launch_bits_gs<4, 64>(V, map, p, grid_y, smem, stream);
+    return launch_bits_gs<4, 64>(V, R, map, p, grid, threads, smem, stream);
 }
 }  // namespace qmv

@@ -6,32 +6,33 @@
 // sketch": scale * accum + sum * bias, no dequantized weight) applied once per
 // group (mlxcel PR #1681, "Not covered"), and its order-preserving streamed
 // form (#1289 "Step 2"): the weights are read and decoded once and reused for
-// V <= 16 activation vectors, with each vector's fp32 operation sequence
+// V <= 16 activation vectors, each vector's fp32 operation sequence being
 // exactly the one an M = 1 launch performs.
 //
-// Work decomposition (nothing here depends on V):
-//  * CTA = 8 warps = 64 consecutive output rows x one K-split (blockIdx.y).
-//  * A warp owns 8 rows. Its lane (p, j), p = lane/8, j = lane%8, owns the row
-//    pair {p, p+4} and slice j: local group 8*t + j of the split in stage t.
-//  * Weights stream through a private ring per warp: 128-byte x 8-row TMA
-//    boxes, 128B-swizzled, one mbarrier per stage; the warp is its own
-//    producer (lane 0 refills a slot after the warp has read it).
-//  * x is staged once per CTA into shared memory as fp32, pre-multiplied by
-//    2^(-bits * (i mod 16/bits)), with a 16-byte pad after each group so the
-//    eight slices read eight different bank groups; sum(x) per group is
-//    staged beside it.
+// Work decomposition (none of it changes the arithmetic):
+//  * a row block is 4R consecutive rows; in the warp processing it, lane
+//    (p, j), p = lane/8, j = lane%8, owns rows {p, p+4, ..., p+4(R-1)} and
+//    slice j of every stage;
+//  * a stage is 8 consecutive groups of the row block, one per slice, brought
+//    into a private ring of the warp by 2-D TMA boxes (128 bytes x 4R rows,
+//    128B-swizzled), one mbarrier per ring slot; lane 0 refills a slot once the
+//    warp has read it;
+//  * a CTA owns row blocks and a range of K-chunks (see Params); x of its chunk
+//    range is staged once into shared memory as fp32, each value
+//    pre-multiplied by 2^(-bits * k) (k = its field position inside a 16-bit
+//    half word) and padded by 16 bytes per group, so the eight slices hit eight
+//    different bank groups; sum(x) per group is staged beside it.
 //
-// Fixed fp32 order for output (m, n) -- the definition the bit-identity rests on:
-//  1. per group: two running sums, even and odd elements, each in increasing
-//     element order: a_e = fma(q_t, x_t, a_e) (t even), a_o likewise (t odd),
-//     starting from +0 (a packed fma.rn.f32x2); d = a_e + a_o.
-//     Products q_t * x_t are exact in fp32 (4-bit integer times 8-bit mantissa).
-//  2. fold: P = fma(s_g, d, P); P = fma(b_g, sx_g, P), where P is the running
-//     value of slice j over its groups j, j+8, j+16, ... in increasing order
-//     and sx_g = (((x_0 + x_1) + x_2) + ...) over the group.
-//  3. slices: butterfly over j with xor 4, 2, 1 (each step P + P').
-//  4. splits: y = ((p_0 + p_1) + p_2) + ... in split order (one split: y = p_0).
-//  5. y rounded once to bf16, nearest even.
+// Fixed fp32 order of output (m, n), for every M:
+//  1. group: two running sums over even and odd elements, each in increasing
+//     order from +0 (one packed fma.rn.f32x2 per element pair): d = a_e + a_o.
+//     Every product q*x is exact in fp32 (small integer times 8-bit mantissa);
+//  2. fold: P = fma(s_g, d, P); P = fma(b_g, sx_g, P), sx_g = eight sums of
+//     eight consecutive x (each left to right) added left to right; P of
+//     slice j runs over groups j, j+8, ... of the chunk in increasing order;
+//  3. chunk value = butterfly over the eight slices (xor 4, 2, 1);
+//  4. y = ((c_0 + c_1) + c_2) + ... over the chunks of kChunkElems elements;
+//  5. one rounding to bf16, nearest even.
 #pragma once
 
 #include <cuda.h>
@@ -72,15 +73,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// One wait attempt: the thread may sleep in the instruction (up to the
+// suspend-time hint, in ns) until the phase completes.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(1000000u)
         : "memory");
     return done != 0;
 }
@@ -92,15 +95,15 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
-// Bounded wait: gives up after ~2 s of wall time or 2^28 polls, whichever
+// Bounded wait: gives up after ~2 s of wall time or 2^24 attempts, whichever
 // comes first, so a lost transfer can never hang the GPU.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1; it < (1u << 28); ++it) {
+    for (uint32_t it = 1; it < (1u << 24); ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0 && global_timer_ns() - t0 > 2000000000ull) return false;
+        if (global_timer_ns() - t0 > 2000000000ull) return false;
     }
     return false;
 }
@@ -134,34 +137,74 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint16_t h)
 // binary32 2^23: OR-ing an integer m < 2^23 into its significand gives 2^23 + m.
 constexpr uint32_t kMagic = 0x4B000000u;
 
-__device__ __forceinline__ float2 magic_pair(uint32_t w, uint32_t mask_lo, uint32_t mask_hi)
+// Pairs of fp32 values travel as one 64-bit register (low half = first
+// element), the operand form of the packed f32x2 instructions.
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c)
 {
-    return make_float2(__uint_as_float((w & mask_lo) | kMagic), __uint_as_float((w & mask_hi) | kMagic));
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ float pair_lo(uint64_t v) { return __uint_as_float(uint32_t(v)); }
+__device__ __forceinline__ float pair_hi(uint64_t v) { return __uint_as_float(uint32_t(v >> 32)); }
+
+// Elements of a packed word at masks MASK_LO and MASK_HI, as the exact pair
+// (q_lo * 2^(bits*k_lo), q_hi * 2^(bits*k_hi)): each field is OR-ed into the
+// significand of 2^23 (one LOP3 each, the mask as immediate, the magic
+// constant in a register) and 2^23 is subtracted from both halves at once.
+template <uint32_t MASK_LO, uint32_t MASK_HI>
+__device__ __forceinline__ uint64_t field_pair(uint32_t w, uint32_t magic, uint64_t neg_magic2)
+{
+    uint64_t d;
+    asm("{\n\t.reg .b32 lo, hi;\n\t.reg .b64 t;\n\t"
+        "lop3.b32 lo, %1, %2, %4, 0xEA;\n\t"
+        "lop3.b32 hi, %1, %3, %4, 0xEA;\n\t"
+        "mov.b64 t, {lo, hi};\n\t"
+        "add.rn.f32x2 %0, t, %5;\n\t}"
+        : "=l"(d)
+        : "r"(w), "n"(MASK_LO), "n"(MASK_HI), "r"(magic), "l"(neg_magic2));
+    return d;
 }
 
 // Element pairs (2p, 2p+1) of one packed word, as exact floats q * 2^(bits*k),
 // k the element's position inside its 16-bit half. The matching x values were
 // staged pre-multiplied by 2^(-bits*k), so each product equals q * x exactly.
 template <int BITS>
-__device__ __forceinline__ void extract_pairs(uint32_t w, float2 (&q)[16 / BITS])
+__device__ __forceinline__ void extract_pairs(uint32_t w, uint32_t magic, uint64_t nm, uint64_t (&q)[16 / BITS])
 {
-    const float2 neg_magic = make_float2(-8388608.0f, -8388608.0f);
-    const uint32_t lo = w, hi = w >> 16;
+    // w >> 16 as a multiply-high, which runs on the FMA pipe (the extraction
+    // keeps the integer/logic pipe busy).
+    uint32_t hi;
+    asm("mul.hi.u32 %0, %1, 65536;" : "=r"(hi) : "r"(w));
+    const uint32_t lo = w;
     if constexpr (BITS == 4) {
-        q[0] = __fadd2_rn(magic_pair(lo, 0x000Fu, 0x00F0u), neg_magic);
-        q[1] = __fadd2_rn(magic_pair(lo, 0x0F00u, 0xF000u), neg_magic);
-        q[2] = __fadd2_rn(magic_pair(hi, 0x000Fu, 0x00F0u), neg_magic);
-        q[3] = __fadd2_rn(magic_pair(hi, 0x0F00u, 0xF000u), neg_magic);
+        q[0] = field_pair<0x000Fu, 0x00F0u>(lo, magic, nm);
+        q[1] = field_pair<0x0F00u, 0xF000u>(lo, magic, nm);
+        q[2] = field_pair<0x000Fu, 0x00F0u>(hi, magic, nm);
+        q[3] = field_pair<0x0F00u, 0xF000u>(hi, magic, nm);
     } else {
-        q[0] = __fadd2_rn(magic_pair(lo, 0x0003u, 0x000Cu), neg_magic);
-        q[1] = __fadd2_rn(magic_pair(lo, 0x0030u, 0x00C0u), neg_magic);
-        q[2] = __fadd2_rn(magic_pair(lo, 0x0300u, 0x0C00u), neg_magic);
-        q[3] = __fadd2_rn(magic_pair(lo, 0x3000u, 0xC000u), neg_magic);
-        q[4] = __fadd2_rn(magic_pair(hi, 0x0003u, 0x000Cu), neg_magic);
-        q[5] = __fadd2_rn(magic_pair(hi, 0x0030u, 0x00C0u), neg_magic);
-        q[6] = __fadd2_rn(magic_pair(hi, 0x0300u, 0x0C00u), neg_magic);
-        q[7] = __fadd2_rn(magic_pair(hi, 0x3000u, 0xC000u), neg_magic);
+        q[0] = field_pair<0x0003u, 0x000Cu>(lo, magic, nm);
+        q[1] = field_pair<0x0030u, 0x00C0u>(lo, magic, nm);
+        q[2] = field_pair<0x0300u, 0x0C00u>(lo, magic, nm);
+        q[3] = field_pair<0x3000u, 0xC000u>(lo, magic, nm);
+        q[4] = field_pair<0x0003u, 0x000Cu>(hi, magic, nm);
+        q[5] = field_pair<0x0030u, 0x00C0u>(hi, magic, nm);
+        q[6] = field_pair<0x0300u, 0x0C00u>(hi, magic, nm);
+        q[7] = field_pair<0x3000u, 0xC000u>(hi, magic, nm);
     }
+}
+
+__device__ __forceinline__ void lds_v2_u64(uint32_t addr, uint64_t &a, uint64_t &b)
+{
+    asm volatile("ld.shared.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
+}
+
+__device__ __forceinline__ uint4 lds_v4_u32(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4 &c, int k)
@@ -171,52 +214,45 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &c, int k)
 
 // ----------------------------------------------------------- group dot --
 
-// Address of 16-byte chunk c of warp-local row r inside a 128B-swizzled box.
-__device__ __forceinline__ const uint4 *box_chunk(const uint8_t *box, int r, int c)
+// Step 1 of the fixed order for one group of the lane's R rows against V
+// staged vectors: acc[r][v] = (a_e, a_o) as one 64-bit pair.
+//   box     shared address of the stage;
+//   woff[r] byte offset in the stage of the first 16-byte chunk of slice j's
+//           group in row pr + 4r (128B swizzle applied; chunk c of the group
+//           sits at woff ^ (c << 4));
+//   xg      shared address of the group's staged x (vector 0); xvstride in bytes.
+template <int BITS, int GS, int V, int R>
+__device__ __forceinline__ void group_dot(uint32_t box, const uint32_t (&woff)[R], uint32_t xg, uint32_t xvstride,
+                                          uint32_t magic, uint64_t nm, uint64_t (&acc)[R][V])
 {
-    return reinterpret_cast<const uint4 *>(box + r * kBoxBytes + ((c ^ (r & 7)) << 4));
-}
-
-// One group of the lane's two rows against V staged vectors: step 1 of the
-// fixed order. acc[r][v] = (a_e, a_o).
-template <int BITS, int GS, int V>
-__device__ __forceinline__ void group_dot(const uint8_t *stage, int j, int rA, int rB, const float *xg,
-                                          int xvstride, float2 (&acc)[2][V])
-{
-    constexpr int kGB = group_bytes(BITS, GS);
-    constexpr int kChunks = kGB / 16;
-    constexpr int kGPB = groups_per_box(BITS, GS);
+    constexpr int kChunks = group_bytes(BITS, GS) / 16;
     constexpr int kPerWord = 32 / BITS;
-    const uint8_t *box = stage + (j / kGPB) * kBoxSmem;
-    const int c0 = (j % kGPB) * kChunks;
 
-    uint4 wa[kChunks], wb[kChunks];
+    uint4 w[R][kChunks];
 #pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
-        wa[c] = *box_chunk(box, rA, c0 + c);
-        wb[c] = *box_chunk(box, rB, c0 + c);
-    }
+    for (int r = 0; r < R; ++r)
 #pragma unroll
-    for (int v = 0; v < V; ++v) {
-        acc[0][v] = make_float2(0.0f, 0.0f);
-        acc[1][v] = make_float2(0.0f, 0.0f);
-    }
+        for (int c = 0; c < kChunks; ++c) w[r][c] = lds_v4_u32(box + (woff[r] ^ (c << 4)));
 #pragma unroll
-    for (int w = 0; w < kChunks * 4; ++w) {
-        float2 qa[kPerWord / 2], qb[kPerWord / 2];
-        extract_pairs<BITS>(word_of(wa[w / 4], w % 4), qa);
-        extract_pairs<BITS>(word_of(wb[w / 4], w % 4), qb);
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[r][v] = 0ull;
+#pragma unroll
+    for (int wi = 0; wi < kChunks * 4; ++wi) {
+        uint64_t q[R][kPerWord / 2];
+#pragma unroll
+        for (int r = 0; r < R; ++r) extract_pairs<BITS>(word_of(w[r][wi / 4], wi % 4), magic, nm, q[r]);
 #pragma unroll
         for (int v = 0; v < V; ++v) {
-            const float4 *xv = reinterpret_cast<const float4 *>(xg + v * xvstride + w * kPerWord);
 #pragma unroll
-            for (int h = 0; h < kPerWord / 4; ++h) {
-                const float4 x4 = xv[h];
-                const float2 x01 = make_float2(x4.x, x4.y), x23 = make_float2(x4.z, x4.w);
-                acc[0][v] = __ffma2_rn(qa[2 * h], x01, acc[0][v]);
-                acc[1][v] = __ffma2_rn(qb[2 * h], x01, acc[1][v]);
-                acc[0][v] = __ffma2_rn(qa[2 * h + 1], x23, acc[0][v]);
-                acc[1][v] = __ffma2_rn(qb[2 * h + 1], x23, acc[1][v]);
+            for (int hh = 0; hh < kPerWord / 4; ++hh) {
+                uint64_t x01, x23;
+                lds_v2_u64(xg + v * xvstride + (wi * kPerWord + hh * 4) * 4, x01, x23);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    acc[r][v] = ffma2(q[r][2 * hh], x01, acc[r][v]);
+                    acc[r][v] = ffma2(q[r][2 * hh + 1], x23, acc[r][v]);
+                }
             }
         }
     }
@@ -224,107 +260,127 @@ __device__ __forceinline__ void group_dot(const uint8_t *stage, int j, int rA, i
 
 // ---------------------------------------------------------------- kernel --
 
-// Position of a warp in its (tile, chunk, stage) sequence. Tiles advance by
-// gridDim.x (persistent CTAs); chunks run over the CTA's chunk range.
-struct Cursor {
-    int tile, chunk, t;
-};
-
-// First group of chunk c (chunk boundaries are box-aligned; see split_count).
-template <int BITS, int GS>
-__device__ __forceinline__ int chunk_first_group(const Params &p, int c)
-{
-    const int g = (c * p.nbox / p.ks) * groups_per_box(BITS, GS);
-    return g < p.G ? g : p.G;
-}
-
-template <int BITS, int GS, int V>
+template <int BITS, int GS, int V, int R>
 __device__ __forceinline__ void qmv_body(const CUtensorMap *tmap_w, const Params &p)
 {
+    constexpr int RW = 4 * R;  // rows per row block (one warp's rows)
+    constexpr int kGB = group_bytes(BITS, GS);
     constexpr int kGPB = groups_per_box(BITS, GS);
     constexpr int kBPS = boxes_per_stage(BITS, GS);
-    constexpr int kStageBytes = stage_bytes(BITS, GS);
-    constexpr int kStages = ring_stages(BITS, GS);
+    constexpr int kCG = chunk_groups(GS);
+    constexpr int kSPC = kCG / kSlices;  // stages per full chunk (4 or 2)
     constexpr int kXS = x_stride(GS);
     constexpr int kPerHalf = 16 / BITS;
-    constexpr int kGB = group_bytes(BITS, GS);
+    constexpr int kBoxSmem = kBoxBytes * RW;
+    constexpr int kStageBytes = kBPS * kBoxSmem;
 
-    extern __shared__ uint8_t smem_raw[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ unsigned s_ticket;
-    __shared__ int s_cg0[kMaxChunksPerCta + 1];  // first group of each chunk of this CTA, and the end
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const SmemLayout L = smem_layout(BITS, GS, V, p.gsm);
+    // Align the dynamic base to 1024 bytes (the 128B swizzle pattern repeats
+    // every 1024 bytes) by offsetting the __shared__ array itself, so every
+    // access below stays a shared-memory access.
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int nwarps = p.warps;
+    const int nthreads = nwarps * 32;
+    const int tile_rows = p.RB * RW;  // rows the CTA's chunk-value buffer holds
+    const SmemLayout L = smem_layout(BITS, GS, V, RW, nwarps, p.stages, p.gsm, p.cps, tile_rows);
     float *xs = reinterpret_cast<float *>(smem + L.xs);
     float *sxs = reinterpret_cast<float *>(smem + L.sx);
+    float *cvs = reinterpret_cast<float *>(smem + L.cv);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int pr = lane >> 3, j = lane & 7;
-    const int chunk_lo = blockIdx.y * p.cps;
-    const int chunk_hi = chunk_lo + p.cps < p.ks ? chunk_lo + p.cps : p.ks;
-    const int ncpc = chunk_hi - chunk_lo;  // chunks of this CTA (<= kMaxChunksPerCta, checked on the host)
-    if (tid <= ncpc) s_cg0[tid] = chunk_first_group<BITS, GS>(p, chunk_lo + tid);
-    __syncthreads();
-    const int g_lo = s_cg0[0];
-    const int gsn = s_cg0[ncpc] - g_lo;  // groups of x staged by this CTA
-    // chunk-local helpers (c is relative to chunk_lo)
-    auto cg0 = [&](int c) { return s_cg0[c]; };
-    auto cstages = [&](int c) { return (s_cg0[c + 1] - s_cg0[c] + kSlices - 1) / kSlices; };
+    const int c_lo = blockIdx.y * p.cps;
+    const int c_hi = c_lo + p.cps < p.ks ? c_lo + p.cps : p.ks;
+    const int ncta = c_hi - c_lo;
+    const int g_lo = c_lo * kCG;
+    const int g_hi = c_hi * kCG < p.G ? c_hi * kCG : p.G;
+    const int gsn = g_hi - g_lo;  // groups of x staged by this CTA
+    // Row blocks of this CTA: a balanced share of all NB row blocks (persistent
+    // grid), or RB consecutive ones (one row tile per CTA).
+    int rb_lo, rb_hi;
+    if (p.balanced) {
+        rb_lo = int((long long)blockIdx.x * p.NB / gridDim.x);
+        rb_hi = int((long long)(blockIdx.x + 1) * p.NB / gridDim.x);
+    } else {
+        rb_lo = blockIdx.x * p.RB;
+        rb_hi = rb_lo + p.RB < p.NB ? rb_lo + p.RB : p.NB;
+    }
+    const int row_t0 = rb_lo * RW;
+    const int nunits = (rb_hi - rb_lo) * p.H;  // (row block, chunk phase) pairs
+    const int stage_shift = __ffs(p.stages) - 1;
 
-    const uint32_t bar0 = smem_u32(bars + warp * kStages);
-    const uint32_t ring_w = smem_u32(smem + L.ring + warp * kRingBytesPerWarp);
+    // A unit is one row block and the contiguous chunk block [cb0, cb1) of its
+    // chunk phase: groups [gw0, gw1), stage s holding groups gw0 + 8s .. + 7; a
+    // chunk ends every kSPC stages and only the unit's last stage can be partial.
+    struct Unit {
+        int row0, cb0, gw0, gw1, total;
+    };
+    auto unit_geo = [&](int u) {
+        Unit q;
+        const int rbl = u / p.H, hh = u - rbl * p.H;
+        q.row0 = (rb_lo + rbl) * RW;
+        q.cb0 = c_lo + hh * ncta / p.H;
+        const int cb1 = c_lo + (hh + 1) * ncta / p.H;
+        q.gw0 = q.cb0 * kCG;
+        q.gw1 = cb1 * kCG < p.G ? cb1 * kCG : p.G;
+        q.total = (q.gw1 - q.gw0 + kSlices - 1) / kSlices;
+        return q;
+    };
+
+    const uint32_t bar0 = smem_u32(bars + warp * p.stages);
+    const uint32_t ring_w = smem_u32(smem + L.ring + warp * p.stages * kStageBytes);
     const uint64_t pol = l2_evict_first_policy();
 
-    auto warp_row0 = [&](int tile) { return tile * kRowsPerCta + warp * kRowsPerWarp; };
-    auto valid = [&](const Cursor &c) { return c.tile < p.ntiles && warp_row0(c.tile) < p.N; };
-    auto advance = [&](Cursor &c) {
-        if (++c.t == cstages(c.chunk)) {
-            c.t = 0;
-            if (++c.chunk == ncpc) {
-                c.chunk = 0;
-                c.tile += gridDim.x;
-            }
-        }
-    };
-    auto issue = [&](const Cursor &c, int slot) {
-        const int gc0 = cg0(c.chunk), gc1 = cg0(c.chunk + 1);
-        const int gl0 = gc0 + c.t * kSlices;
-        int nb = (gc1 - gl0 + kGPB - 1) / kGPB;
+    // Producer (lane 0): the warp's stage sequence runs through its units
+    // u = warp, warp + nwarps, ... in order; `issued` counts stages issued.
+    int pu = warp, ps = 0, issued = 0;
+    Unit pg = unit_geo(pu < nunits ? pu : 0);
+    auto issue_next = [&]() {
+        if (pu >= nunits) return;
+        const int slot = issued & (p.stages - 1);
+        const int gst = pg.gw0 + ps * kSlices;  // first group of the stage
+        int nb = (pg.gw1 - gst + kGPB - 1) / kGPB;
         nb = nb < kBPS ? nb : kBPS;
         mbar_arrive_expect_tx(bar0 + 8 * slot, nb * kBoxSmem);
         for (int b = 0; b < nb; ++b)
-            tma_load_2d(ring_w + slot * kStageBytes + b * kBoxSmem, tmap_w, gl0 * kGB + b * kBoxBytes,
-                        warp_row0(c.tile), bar0 + 8 * slot, pol);
+            tma_load_2d(ring_w + slot * kStageBytes + b * kBoxSmem, tmap_w, gst * kGB + b * kBoxBytes, pg.row0,
+                        bar0 + 8 * slot, pol);
+        ++issued;
+        if (++ps == pg.total) {
+            ps = 0;
+            pu += nwarps;
+            if (pu < nunits) pg = unit_geo(pu);
+        }
     };
 
     // Weight tiles first: they do not depend on x, so their latency overlaps the staging below.
-    Cursor prod = {int(blockIdx.x), 0, 0};
-    int issued = 0;
     if (lane == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
+        for (int s = 0; s < p.stages; ++s) mbar_init(bar0 + 8 * s, 1);
         fence_mbar_init();
-        for (; issued < kStages && valid(prod); ++issued, advance(prod)) issue(prod, issued);
+        for (int s = 0; s < p.stages; ++s) issue_next();
     }
     __syncwarp();
 
-    // Stage x for groups [g_lo, g_lo + gsn): fp32, position-scaled, 8 elements per task.
+    // Stage x for groups [g_lo, g_hi): fp32, position-scaled, 8 elements per task.
     {
         constexpr int kUPG = GS / 8;
-        const int per_vec = gsn * kUPG, total = V * per_vec;
-        for (int u0 = tid; u0 < total; u0 += 4 * kThreads) {
+        const int per_vec = gsn * kUPG, all = V * per_vec;
+        for (int u0 = tid; u0 < all; u0 += 4 * nthreads) {
             uint4 raw[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const int u = u0 + k * kThreads;
-                if (u < total) {
+                const int u = u0 + k * nthreads;
+                if (u < all) {
                     const int v = u / per_vec, rem = u - v * per_vec;
                     raw[k] = __ldg(reinterpret_cast<const uint4 *>(p.x + size_t(v) * p.K + size_t(g_lo) * GS) + rem);
                 }
             }
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const int u = u0 + k * kThreads;
-                if (u < total) {
+                const int u = u0 + k * nthreads;
+                if (u < all) {
                     const int v = u / per_vec, rem = u - v * per_vec;
                     const int gl = rem / kUPG, e8 = rem - gl * kUPG;
                     const uint32_t w4[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
@@ -342,8 +398,8 @@ __device__ __forceinline__ void qmv_body(const CUtensorMap *tmap_w, const Params
             }
         }
         // sum(x) per (vector, group): eight sums of eight consecutive elements,
-        // each left to right, then those eight (sixteen for gs=128) left to right.
-        for (int idx = tid; idx < V * gsn; idx += kThreads) {
+        // each left to right, then those (eight, or sixteen for gs = 128) left to right.
+        for (int idx = tid; idx < V * gsn; idx += nthreads) {
             const int v = idx / gsn, gl = idx - v * gsn;
             const uint4 *src = reinterpret_cast<const uint4 *>(p.x + size_t(v) * p.K + size_t(g_lo + gl) * GS);
             uint4 raw[kUPG];
@@ -364,173 +420,185 @@ __device__ __forceinline__ void qmv_body(const CUtensorMap *tmap_w, const Params
     }
     __syncthreads();
 
+    bool ok = true;
+    int consumed = 0;
+    // The magic constant and the pair (-2^23, -2^23) as register operands of the extraction.
+    uint32_t magic;
+    asm volatile("mov.b32 %0, %1;" : "=r"(magic) : "n"(kMagic));
+    const uint64_t nm = 0xCB000000CB000000ull;
+    // Per-lane byte offsets, inside a stage, of the first chunk of slice j's
+    // group for each of the lane's rows (128B swizzle: chunk index XOR row % 8).
+    uint32_t woff[R];
+    {
+        constexpr int kChunks = kGB / 16;
+        const int c0 = (j % kGPB) * kChunks;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int row = pr + 4 * r;
+            woff[r] = uint32_t((j / kGPB) * kBoxSmem + row * kBoxBytes + ((c0 ^ (row & 7)) << 4));
+        }
+    }
+    const uint32_t ring_s = smem_u32(smem + L.ring);
+    const uint32_t xs_s = smem_u32(xs);
+
+    for (int u = warp; u < nunits && ok; u += nwarps) {
+        const Unit q = unit_geo(u);
+        const int rbl = u / p.H;
+        // Scale and bias of the lane's group, loaded one stage ahead.
+        const uint16_t *srow[R], *brow[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int n = q.row0 + pr + 4 * r < p.N ? q.row0 + pr + 4 * r : p.N - 1;
+            srow[r] = p.scales + size_t(n) * p.G;
+            brow[r] = p.biases + size_t(n) * p.G;
+        }
+        uint16_t ms[R], mb[R];
+        {
+            const int g = q.gw0 + j < q.gw1 ? q.gw0 + j : q.gw1 - 1;
+#pragma unroll
+            for (int r = 0; r < R; ++r) { ms[r] = __ldg(srow[r] + g); mb[r] = __ldg(brow[r] + g); }
+        }
+        float part[R][V];
+        for (int s = 0; s < q.total; ++s) {
+            const int t = s & (kSPC - 1);
+            if (t == 0) {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int v = 0; v < V; ++v) part[r][v] = 0.0f;
+            }
+            float fs[R], fb[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) { fs[r] = bf16_bits_to_f32(ms[r]); fb[r] = bf16_bits_to_f32(mb[r]); }
+            const int g = q.gw0 + s * kSlices + j;
+            if (s + 1 < q.total) {
+                const int gn = g + kSlices < q.gw1 ? g + kSlices : q.gw1 - 1;
+#pragma unroll
+                for (int r = 0; r < R; ++r) { ms[r] = __ldg(srow[r] + gn); mb[r] = __ldg(brow[r] + gn); }
+            }
+            const int slot = consumed & (p.stages - 1);
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar0 + 8 * slot, (consumed >> stage_shift) & 1));
+            if (!ok) break;
+            if (g < q.gw1) {
+                const int gl = g - g_lo;
+                uint64_t acc[R][V];
+                group_dot<BITS, GS, V, R>(ring_s + (warp * p.stages + slot) * kStageBytes, woff,
+                                          xs_s + gl * kXS * 4, p.gsm * kXS * 4, magic, nm, acc);
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    const float sx = sxs[v * p.gsm + gl];
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const float d = __fadd_rn(pair_lo(acc[r][v]), pair_hi(acc[r][v]));
+#if defined(QMV_TEST_MUTATE_ORDER)
+                        // Test-only build: the streamed kernel folds bias before scale,
+                        // so the bit-identity tests can show they detect an order change.
+                        if constexpr (V > 1) {
+                            part[r][v] = __fmaf_rn(fb[r], sx, part[r][v]);
+                            part[r][v] = __fmaf_rn(fs[r], d, part[r][v]);
+                            continue;
+                        }
+#endif
+                        part[r][v] = __fmaf_rn(fs[r], d, part[r][v]);
+                        part[r][v] = __fmaf_rn(fb[r], sx, part[r][v]);
+                    }
+                }
+            }
+            __syncwarp();
+            ++consumed;
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue_next();
+            }
+            // End of a chunk: butterfly over the slices, chunk value to shared memory.
+            if (t == kSPC - 1 || s == q.total - 1) {
+                float *cv = cvs + ((q.cb0 + s / kSPC - c_lo) * tile_rows + rbl * RW) * V;
+#pragma unroll
+                for (int v = 0; v < V; ++v)
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        float x1 = part[r][v];
+                        x1 = __fadd_rn(x1, __shfl_xor_sync(0xffffffffu, x1, 4));
+                        x1 = __fadd_rn(x1, __shfl_xor_sync(0xffffffffu, x1, 2));
+                        x1 = __fadd_rn(x1, __shfl_xor_sync(0xffffffffu, x1, 1));
+                        if ((v & 7) == j) cv[(pr + 4 * r) * V + v] = x1;
+                    }
+            }
+        }
+    }
+    if (!ok && lane == 0) {
+        // Record the failure, then wait (bounded) for this warp's own copies
+        // still in flight before the CTA may exit.
+        atomicOr(p.err, 1u);
+        for (int s2 = consumed; s2 < issued; ++s2)
+            (void)mbar_wait_bounded(bar0 + 8 * (s2 & (p.stages - 1)), (s2 >> stage_shift) & 1);
+    }
+    __syncthreads();
+
     auto store_y = [&](int v, int n, float val) {
         if (p.f32_out)
             static_cast<float *>(p.y)[size_t(v) * p.N + n] = val;
         else
             static_cast<__nv_bfloat16 *>(p.y)[size_t(v) * p.N + n] = __float2bfloat16_rn(val);
     };
+    const int nrows = (rb_hi - rb_lo) * RW;
 
-    const int rA = pr, rB = pr + 4;
-    int consumed = 0;
-    bool ok = true;
-    // Metadata (scale, bias) of the lane's group one stage ahead of the weights.
-    Cursor meta = {int(blockIdx.x), 0, 0};
-    uint16_t msA = 0, mbA = 0, msB = 0, mbB = 0;
-    auto load_meta = [&](const Cursor &c) {
-        if (!valid(c)) return;
-        const int gc0 = cg0(c.chunk), gc1 = cg0(c.chunk + 1);
-        int g = gc0 + c.t * kSlices + j;
-        g = g < gc1 ? g : gc1 - 1;
-        const int r0 = warp_row0(c.tile);
-        const int nA = r0 + rA < p.N ? r0 + rA : p.N - 1;
-        const int nB = r0 + rB < p.N ? r0 + rB : p.N - 1;
-        msA = __ldg(p.scales + size_t(nA) * p.G + g);
-        mbA = __ldg(p.biases + size_t(nA) * p.G + g);
-        msB = __ldg(p.scales + size_t(nB) * p.G + g);
-        mbB = __ldg(p.biases + size_t(nB) * p.G + g);
-    };
-    load_meta(meta);
-
-    for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
-        const int row0 = warp_row0(tile);
-        const bool active = row0 < p.N;
-        const int nA = row0 + rA, nB = row0 + rB;
-        float yr[2][V];
-        if (active && ok) {
-            for (int c = 0; c < ncpc; ++c) {
-                const int gc0 = cg0(c), gc1 = cg0(c + 1);
-                const int nst = (gc1 - gc0 + kSlices - 1) / kSlices;
-                float part[2][V];
-#pragma unroll
-                for (int v = 0; v < V; ++v) part[0][v] = part[1][v] = 0.0f;
-                for (int t = 0; t < nst; ++t) {
-                    const int slot = consumed % kStages;
-                    const uint32_t parity = (consumed / kStages) & 1;
-                    const float fsA = bf16_bits_to_f32(msA), fbA = bf16_bits_to_f32(mbA);
-                    const float fsB = bf16_bits_to_f32(msB), fbB = bf16_bits_to_f32(mbB);
-                    advance(meta);
-                    load_meta(meta);
-                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar0 + 8 * slot, parity));
-                    if (!ok) break;
-                    const int g = gc0 + t * kSlices + j;
-                    if (g < gc1) {
-                        const int gl = g - g_lo;
-                        float2 acc[2][V];
-                        group_dot<BITS, GS, V>(smem + L.ring + warp * kRingBytesPerWarp + slot * kStageBytes, j, rA,
-                                               rB, xs + gl * kXS, p.gsm * kXS, acc);
-#pragma unroll
-                        for (int v = 0; v < V; ++v) {
-                            const float sx = sxs[v * p.gsm + gl];
-#if defined(QMV_TEST_MUTATE_ORDER)
-                            // Test-only build: the streamed kernel folds bias before scale,
-                            // so the bit-identity tests can show they detect an order change.
-                            if constexpr (V > 1) {
-                                part[0][v] = __fmaf_rn(fbA, sx, part[0][v]);
-                                part[0][v] = __fmaf_rn(fsA, __fadd_rn(acc[0][v].x, acc[0][v].y), part[0][v]);
-                                part[1][v] = __fmaf_rn(fbB, sx, part[1][v]);
-                                part[1][v] = __fmaf_rn(fsB, __fadd_rn(acc[1][v].x, acc[1][v].y), part[1][v]);
-                                continue;
-                            }
-#endif
-                            part[0][v] = __fmaf_rn(fsA, __fadd_rn(acc[0][v].x, acc[0][v].y), part[0][v]);
-                            part[0][v] = __fmaf_rn(fbA, sx, part[0][v]);
-                            part[1][v] = __fmaf_rn(fsB, __fadd_rn(acc[1][v].x, acc[1][v].y), part[1][v]);
-                            part[1][v] = __fmaf_rn(fbB, sx, part[1][v]);
-                        }
-                    }
-                    __syncwarp();
-                    ++consumed;
-                    if (lane == 0 && valid(prod)) {
-                        fence_proxy_async_smem();
-                        issue(prod, issued % kStages);
-                        ++issued;
-                        advance(prod);
-                    }
-                }
-                if (!ok) break;
-                // Step 3: butterfly over the slices; step 4: left fold over chunks.
-#pragma unroll
-                for (int v = 0; v < V; ++v)
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        float t = part[r][v];
-                        t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 4));
-                        t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 2));
-                        t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 1));
-                        yr[r][v] = c == 0 ? t : __fadd_rn(yr[r][v], t);
-                    }
-            }
+    // Step 4: fold the chunk values left to right.
+    if (p.cps == p.ks) {
+        for (int idx = tid; idx < nrows * V; idx += nthreads) {
+            const int r = idx / V, v = idx - r * V;
+            const int n = row_t0 + r;
+            if (n >= p.N) continue;
+            float acc = cvs[r * V + v];
+            for (int c = 1; c < p.ks; ++c) acc = __fadd_rn(acc, cvs[(c * tile_rows + r) * V + v]);
+            store_y(v, n, acc);
         }
-
-        if (p.cps == p.ks) {
-            if (active && ok) {
-#pragma unroll
-                for (int v = 0; v < V; ++v)
-                    if ((v & 7) == j) {
-                        if (nA < p.N) store_y(v, nA, yr[0][v]);
-                        if (nB < p.N) store_y(v, nB, yr[1][v]);
-                    }
-            }
-            continue;
-        }
-
-        // One chunk per CTA: publish it; the CTA that completes the row tile
-        // last folds the chunk values left to right and zeroes what it read,
-        // so (with the self-resetting counter) the workspace is zero again.
-        if (active && ok) {
-#pragma unroll
-            for (int v = 0; v < V; ++v)
-                if ((v & 7) == j) {
-                    float *pp = p.partials + (size_t(chunk_lo) * V + v) * p.N;
-                    if (nA < p.N) __stcg(pp + nA, yr[0][v]);
-                    if (nB < p.N) __stcg(pp + nB, yr[1][v]);
-                }
-        }
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) s_ticket = atomicInc(p.counters + tile, unsigned(p.ks - 1));
-        __syncthreads();
-        if (s_ticket == unsigned(p.ks - 1)) {
-            __threadfence();
-            for (int idx = tid; idx < kRowsPerCta * V; idx += kThreads) {
-                const int r = idx % kRowsPerCta, v = idx / kRowsPerCta;
-                const int n = tile * kRowsPerCta + r;
-                if (n >= p.N) continue;
-                float *pp = p.partials + size_t(v) * p.N + n;
-                float acc = __ldcg(pp);
-                __stcg(pp, 0.0f);
-                for (int s = 1; s < p.ks; ++s) {
-                    float *ps = pp + size_t(s) * V * p.N;
-                    acc = __fadd_rn(acc, __ldcg(ps));
-                    __stcg(ps, 0.0f);
-                }
-                store_y(v, n, acc);
-            }
-        }
-        __syncthreads();  // s_ticket is rewritten for the next tile
+        return;
     }
 
-    if (!ok) {
-        // Record the failure, then wait (bounded) for this warp's own copies
-        // still in flight before the CTA exits.
-        if (lane == 0) atomicOr(p.err, 1u);
-        for (int s2 = consumed; s2 < issued; ++s2)
-            (void)mbar_wait_bounded(bar0 + 8 * (s2 % kStages), (s2 / kStages) & 1);
+    // One chunk per CTA: publish its values; the CTA that completes the row
+    // tile last folds all chunks left to right and zeroes what it read, so
+    // (with the self-resetting counter) the workspace is zero again.
+    for (int idx = tid; idx < nrows * V; idx += nthreads) {
+        const int r = idx / V, v = idx - r * V;
+        const int n = row_t0 + r;
+        if (n < p.N) __stcg(p.partials + (size_t(c_lo) * V + v) * p.N + n, cvs[r * V + v]);
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_ticket = atomicInc(p.counters + blockIdx.x, unsigned(p.ks - 1));
+    __syncthreads();
+    if (s_ticket != unsigned(p.ks - 1)) return;
+    __threadfence();
+    for (int idx = tid; idx < nrows * V; idx += nthreads) {
+        const int r = idx % nrows, v = idx / nrows;
+        const int n = row_t0 + r;
+        if (n >= p.N) continue;
+        float *pp = p.partials + size_t(v) * p.N + n;
+        float acc = __ldcg(pp);
+        __stcg(pp, 0.0f);
+        for (int c = 1; c < p.ks; ++c) {
+            float *pc = pp + size_t(c) * V * p.N;
+            acc = __fadd_rn(acc, __ldcg(pc));
+            __stcg(pc, 0.0f);
+        }
+        store_y(v, n, acc);
     }
 }
 
-template <int BITS, int GS>
-__global__ void __launch_bounds__(kThreads, 2) qmv_m1(const __grid_constant__ CUtensorMap tmap_w, const Params p)
+// Rows per lane R: the single-vector kernel comes with R = 2 and R = 4 (the
+// host picks by shape); the streamed kernel uses R = 2 (its registers go to V).
+template <int BITS, int GS, int R>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_m1(const __grid_constant__ CUtensorMap tmap_w, const Params p)
 {
-    qmv_body<BITS, GS, 1>(&tmap_w, p);
+    qmv_body<BITS, GS, 1, R>(&tmap_w, p);
 }
 
 template <int BITS, int GS, int V>
-__global__ void __launch_bounds__(kThreads, (V <= 4 ? 2 : 1))
+__global__ void __launch_bounds__(kMaxWarps * 16, (V <= 4 ? 2 : 1))
     qmv_streamed(const __grid_constant__ CUtensorMap tmap_w, const Params p)
 {
-    qmv_body<BITS, GS, V>(&tmap_w, p);
+    qmv_body<BITS, GS, V, 2>(&tmap_w, p);
 }
 
 }  // namespace qmv

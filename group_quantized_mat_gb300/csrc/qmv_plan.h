@@ -1,106 +1,45 @@
 // Problem geometry shared by the host launcher and the kernels.
 //
-// The K-split count and every split boundary are functions of (K, bits,
-// group_size) alone. They fix the fp32 summation order of each output, so
-// they must never depend on M: that is what keeps column j of an M-vector
-// call bit-identical to an M = 1 call on the same vector (mlxcel issue #1289,
-// "The observation this rests on").
+// The fp32 summation order of an output is fixed by the group size and the
+// K-chunks below, which depend on K and group_size alone. They never depend on
+// M, on the CTA shape or on the GPU: that is what keeps column j of an
+// M-vector call bit-identical to an M = 1 call on the same vector (mlxcel
+// issue #1289, "The observation this rests on").
 #pragma once
 
 #include <cstdint>
 
 namespace qmv {
 
-constexpr int kWarps = 8;                      // warps per CTA
-constexpr int kThreads = kWarps * 32;          // 256
-constexpr int kRowsPerWarp = 8;                // one TMA box is 8 rows tall
-constexpr int kRowsPerCta = kWarps * kRowsPerWarp;  // 64
-constexpr int kSlices = 8;                     // lanes sharing a row pair; one group each per stage
-constexpr int kBoxBytes = 128;                 // TMA box inner extent (bytes) = 128B swizzle span
-constexpr int kBoxSmem = kBoxBytes * kRowsPerWarp;  // 1024 bytes per box in shared memory
-constexpr int kRingBytesPerWarp = 8192;        // weight tiles in flight per warp
-constexpr int kMaxSplitElems = 2048;           // K elements per split, at most
+constexpr int kSlices = 8;          // lanes sharing a row; slice j takes groups j, j+8, ... of a chunk
+constexpr int kChunkElems = 2048;   // K elements per chunk (the last chunk of a row may be shorter)
+constexpr int kBoxBytes = 128;      // TMA box inner extent = 128B swizzle span
 constexpr int kMaxM = 16;
-constexpr int kMaxChunksPerCta = 64;           // a CTA that takes all of K holds at most this many chunks
+constexpr int kMaxWarps = 16;       // warps per CTA
+constexpr int kMaxChunksPerCta = 64;
 
 __host__ __device__ constexpr int group_bytes(int bits, int gs) { return gs * bits / 8; }
 __host__ __device__ constexpr int groups_per_box(int bits, int gs) { return kBoxBytes / group_bytes(bits, gs); }
-__host__ __device__ constexpr int boxes_per_stage(int bits, int gs)
-{
-    return kSlices * group_bytes(bits, gs) / kBoxBytes;
-}
-__host__ __device__ constexpr int stage_bytes(int bits, int gs) { return boxes_per_stage(bits, gs) * kBoxSmem; }
-__host__ __device__ constexpr int ring_stages(int bits, int gs) { return kRingBytesPerWarp / stage_bytes(bits, gs); }
-__host__ __device__ constexpr int x_stride(int gs) { return gs + 4; }  // floats per group, padded
+__host__ __device__ constexpr int boxes_per_stage(int bits, int gs) { return kSlices * group_bytes(bits, gs) / kBoxBytes; }
+__host__ __device__ constexpr int chunk_groups(int gs) { return kChunkElems / gs; }  // a multiple of kSlices
+__host__ __device__ constexpr int x_stride(int gs) { return gs + 4; }               // floats per staged group
 
-// Number of 128-byte weight boxes along one row (the last may be partial).
-inline int row_boxes(int K, int bits, int gs)
+// Number of K-chunks of a row: ceil(G / chunk_groups).
+__host__ __device__ inline int chunk_count(int K, int gs)
 {
     const int G = K / gs;
-    const int gpb = groups_per_box(bits, gs);
-    return (G + gpb - 1) / gpb;
-}
-
-// K-split count: the fewest splits that keep each split within kMaxSplitElems,
-// raised to the next divisor of the box count (equal splits) when one exists
-// below twice that minimum.
-inline int split_count(int K, int bits, int gs)
-{
-    const int nbox = row_boxes(K, bits, gs);
-    int max_boxes = (kMaxSplitElems / gs) / groups_per_box(bits, gs);
-    if (max_boxes < 1) max_boxes = 1;
-    const int ks_min = (nbox + max_boxes - 1) / max_boxes;
-    for (int ks = ks_min; ks <= 2 * ks_min && ks <= nbox; ++ks)
-        if (nbox % ks == 0) return ks;
-    return ks_min;
-}
-
-// Split s covers boxes [s*nbox/ks, (s+1)*nbox/ks) of every row.
-__host__ __device__ inline int split_box_begin(int s, int nbox, int ks)
-{
-    return int((long long)s * nbox / ks);
-}
-
-// Most groups any split holds (sizes the activation staging buffer).
-inline int max_split_groups(int K, int bits, int gs)
-{
-    const int nbox = row_boxes(K, bits, gs), ks = split_count(K, bits, gs);
-    const int gpb = groups_per_box(bits, gs), G = K / gs;
-    int best = 0;
-    for (int s = 0; s < ks; ++s) {
-        int g0 = split_box_begin(s, nbox, ks) * gpb;
-        int g1 = split_box_begin(s + 1, nbox, ks) * gpb;
-        if (g1 > G) g1 = G;
-        if (g1 - g0 > best) best = g1 - g0;
-    }
-    return best;
-}
-
-struct SmemLayout {
-    int ring, xs, sx, bar, total;  // byte offsets from the 1024-aligned base, and the size to request
-};
-
-// gsm: the most groups of x one CTA stages (all of K, or one chunk).
-__host__ __device__ inline SmemLayout smem_layout(int bits, int gs, int V, int gsm)
-{
-    SmemLayout L;
-    L.ring = 0;
-    L.xs = kWarps * kRingBytesPerWarp;
-    L.sx = L.xs + V * gsm * x_stride(gs) * 4;
-    L.bar = (L.sx + V * gsm * 4 + 15) & ~15;
-    const int end = L.bar + kWarps * ring_stages(bits, gs) * 8;
-    L.total = end + 1024;  // slack for aligning the dynamic base to 1024 bytes
-    return L;
+    return (G + chunk_groups(gs) - 1) / chunk_groups(gs);
 }
 
 // Kernel arguments other than the weight tensor map.
 //
-// K is cut into `ks` chunks (the splits above). The chunks fix the order of
-// the fp32 sum; how they are shared out is free: a CTA processes the chunks
-// [blockIdx.y * cps, blockIdx.y * cps + cps), with cps = ks (one CTA sees all
-// of K and folds the chunk values in registers) or cps = 1 (one chunk per
-// CTA; the chunk values meet in the workspace and the CTA that finishes a row
-// tile last folds them). Both give the same bits.
+// A CTA owns up to RB row blocks (4R rows each) and the chunks
+// [blockIdx.y * cps, blockIdx.y * cps + cps). Its work units are (row block,
+// chunk phase) pairs, a chunk phase being one of H contiguous blocks of the
+// CTA's chunks; warp w processes units w, w + warps, ... Chunk values meet in
+// shared memory; with cps = ks the CTA folds them into y, otherwise they go
+// through the workspace and the CTA that completes a row tile last folds all
+// ks of them.
 struct Params {
     const uint16_t *scales;   // bf16 bits [N, G]
     const uint16_t *biases;   // bf16 bits [N, G]
@@ -109,7 +48,42 @@ struct Params {
     float *partials;          // [ks, V, N] when cps < ks
     unsigned *counters;       // [ntiles] when cps < ks, zero between calls
     unsigned *err;            // device error word
-    int N, K, G, ks, nbox, cps, gsm, ntiles, f32_out;
+    int N, K, G;
+    int ks;                   // chunks per row
+    int cps;                  // chunks per CTA: ks or 1
+    int RB, H;                // row blocks (at most) and chunk phases per CTA
+    int warps;                // warps per CTA; warp w takes units w, w + warps, ...
+    int NB;                   // row blocks of the matrix (ceil(N / rows per block))
+    int balanced;             // 1: CTA i takes row blocks [i*NB/grid, (i+1)*NB/grid)
+    int stages;               // weight stages in flight per warp (a power of two)
+    int gsm;                  // groups of x one CTA stages (its chunk range)
+    int ntiles;               // row tiles (counters) when cps < ks
+    int f32_out;
 };
+
+// Shared memory of one CTA, as byte offsets from a 1024-aligned base.
+struct SmemLayout {
+    int ring, xs, sx, cv, bar, total;
+};
+
+// rows_per_block = 4 * R; one stage = boxes_per_stage boxes of (128 B x rows_per_block).
+__host__ __device__ inline int stage_bytes(int bits, int gs, int rows_per_block)
+{
+    return boxes_per_stage(bits, gs) * kBoxBytes * rows_per_block;
+}
+
+__host__ __device__ inline SmemLayout smem_layout(int bits, int gs, int V, int rows_per_block, int warps, int stages,
+                                                  int gsm, int cps, int tile_rows)
+{
+    SmemLayout L;
+    L.ring = 0;
+    L.xs = warps * stages * stage_bytes(bits, gs, rows_per_block);
+    L.sx = L.xs + V * gsm * x_stride(gs) * 4;
+    L.cv = L.sx + V * gsm * 4;
+    L.bar = (L.cv + cps * tile_rows * V * 4 + 15) & ~15;
+    const int end = L.bar + warps * stages * 8;
+    L.total = end + 1024;  // slack for aligning the dynamic base to 1024 bytes
+    return L;
+}
 
 }  // namespace qmv

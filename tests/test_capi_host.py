@@ -90,19 +90,24 @@ def test_pack_rejects_bad_input(lib):
 
 
 def test_split_plan(lib):
-    # the K-split count is a function of K, bits and group size only
-    assert g.qmv_split_count(15360, 3840, 4, 64) == g.qmv_split_count(7, 3840, 4, 64) == 3
+    # K-chunks of 2048 elements: a function of K and the group size only
+    assert g.qmv_split_count(15360, 3840, 4, 64) == g.qmv_split_count(7, 3840, 4, 64) == 2
+    assert g.qmv_split_count(15360, 3840, 2, 64) == 2
+    assert g.qmv_split_count(15360, 3840, 2, 128) == 2
     assert g.qmv_split_count(256, 1024, 4, 64) == 1
-    assert g.qmv_split_count(3840, 15360, 4, 64) == 10
+    assert g.qmv_split_count(3840, 15360, 4, 64) == 8
+    assert g.qmv_split_count(5120, 17408, 4, 64) == 9
     assert g.qmv_split_count(1, 1000, 4, 64) == 0
     assert g.qmv_workspace_size(1, 256, 1024, 4, 64) == 0
     # M = 1: x of all of K fits in one CTA's shared memory, so one CTA folds
-    # every chunk of a row tile itself and no workspace is needed
+    # every chunk of its rows itself and no workspace is needed
     assert g.qmv_workspace_size(1, 15360, 3840, 4, 64) == 0
-    # M = 13: one chunk per CTA; chunk values meet in the workspace
+    # M = 13 / 16: one chunk per CTA; chunk values meet in the workspace after
+    # a 256-byte-aligned block of per-tile counters
     w13 = g.qmv_workspace_size(13, 15360, 3840, 4, 64)
-    assert w13 == 1024 + 3 * 13 * 15360 * 4
-    assert g.qmv_workspace_size(16, 15360, 3840, 4, 64) == 1024 + 3 * 16 * 15360 * 4
+    w16 = g.qmv_workspace_size(16, 15360, 3840, 4, 64)
+    assert w13 > 2 * 13 * 15360 * 4 and (w13 - 2 * 13 * 15360 * 4) % 256 == 0
+    assert w16 - w13 == 2 * 3 * 15360 * 4
     assert g.qmv_workspace_size(17, 15360, 3840, 4, 64) == 0
 
 

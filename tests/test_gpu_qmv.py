@@ -36,12 +36,12 @@ def o():
 
 
 # ----------------------------------------------------------- full parity --
-# Sizes the oracle finishes in seconds that span several row tiles, several
-# K-splits and ragged tails (N not a multiple of 64 or 8; partial last stage).
+# Sizes the oracle finishes in seconds that span several row blocks, several
+# K-chunks and ragged tails (N not a multiple of 8; partial last stage).
 MEDIUM = [
     (256, 1024, 1, 4, 64),      # the tiny workload
-    (200, 3840, 3, 4, 64),      # K of the 12B projection: 3 splits, 7.5 stages each side
-    (130, 15360, 2, 4, 64),     # K of the down projection: 10 splits
+    (200, 3840, 3, 4, 64),      # K of the 12B projection: 2 chunks, 7.5 stages
+    (130, 15360, 2, 4, 64),     # K of the down projection: 8 chunks
     (77, 5120, 16, 4, 64),      # widest M
     (300, 3840, 13, 2, 64),
     (150, 3840, 5, 2, 128),
@@ -49,7 +49,7 @@ MEDIUM = [
     (9, 384, 1, 4, 128),        # one partial box per row
     (1, 64, 1, 4, 64),          # a single group and a single row
     (65, 128, 7, 2, 128),
-    (64, 17408, 2, 4, 64),      # 17 splits
+    (64, 17408, 2, 4, 64),      # 9 chunks, the last one short
 ]
 
 
