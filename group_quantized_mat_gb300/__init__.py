@@ -24,6 +24,7 @@ LIB_PATH = os.path.join(_PKG, "_build", "libqmv.so")
 QMV_MAX_M = 16
 F32_OUT = 0x1
 FORCE_M1_PER_COLUMN = 0x2
+PDL = 0x4
 
 STATUS = {
     0: "QMV_OK", 1: "QMV_ERR_NULL", 2: "QMV_ERR_BITS", 3: "QMV_ERR_GROUP", 4: "QMV_ERR_SHAPE",

@@ -1,7 +1,7 @@
 // Host side of the C ABI declared in include/qmv.h: argument validation, the
-// launch plan (fixed K-chunks, CTA shape), workspace handling, the weight
-// tensor map, and dispatch to the kernels (M = 1 -> qmv_m1, M = 2..16 ->
-// qmv_streamed with V = M).
+// launch plan (fixed K-chunks, CTA shape, unit and ring geometry), workspace
+// handling, the scale/bias tensor maps, and dispatch to the kernels (M = 1 ->
+// qmv_m1, M = 2..16 -> qmv_streamed with V = M).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -47,139 +47,153 @@ qmv_status check_shape(int M, int N, int K, int bits, int gs, bool check_m)
     if (bits != 2 && bits != 4) return QMV_ERR_BITS;
     if (gs != 64 && gs != 128) return QMV_ERR_GROUP;
     if (N < 1 || N > (1 << 30) || K < 1 || K % gs != 0 || K > (1 << 24)) return QMV_ERR_SHAPE;
+    // scale / bias element indices and weight byte offsets stay within 31 and 47 bits
+    if ((long long)N * (K / gs) >= (1ll << 31)) return QMV_ERR_SHAPE;
     if (check_m && (M < 1 || M > QMV_MAX_M)) return QMV_ERR_M_RANGE;
     return QMV_OK;
 }
 
 struct Problem {
-    int M, N, K, bits, gs, G;
-    int ks;         // K-chunks per row (fixes the order; a function of K and gs only)
-    int V;          // vectors per launch
-    int RW;         // rows per row block (one warp's rows)
-    int cps;        // chunks per CTA: ks (all of K) or 1
-    int RB, H;      // row blocks (at most) and chunk phases per CTA
-    int warps;      // warps per CTA
-    int NB;         // row blocks of the matrix
-    int balanced;   // persistent grid with an even share of row blocks per CTA
-    int grid_x;     // CTAs along the rows
-    int stages;     // weight stages in flight per warp
-    int gsm;        // groups of x staged per CTA
-    int tile_rows, ntiles;
+    int V, N, K, bits, gs, G;
+    int S_row;      // 64-element subgroups per row
+    int ks;         // K-chunks per row (fixes the order; a function of K only)
+    int row_bytes;
+    int NB;         // row blocks of 4 rows
+    int cpc;        // chunks per CTA
+    int nranges;    // chunk ranges (grid.y)
+    int grid_rows;  // CTAs along the rows (grid.x)
+    int max_rb;     // row blocks of the largest CTA share
+    int uc;         // chunks per unit
+    int full_rows;  // units are whole rows (one contiguous copy)
+    int pitch;      // bytes per unit row in a ring slot
+    int sb_mode_unit, sbox;
+    int slots, consumers, threads;
     int smem;       // dynamic shared memory per CTA
 };
 
 // Largest dynamic shared memory a CTA may use (static shared memory and
 // reserved bytes kept aside).
-constexpr int kSmemBudget = 227 * 1024 - 256;
-// CTA count below which row tiles are halved to spread the work (about two per SM).
-constexpr int kMinCtas = 304;
+constexpr int kSmemBudget = 227 * 1024 - 512;
+// Staged x of one CTA at most (the rest of shared memory feeds the weight ring).
+constexpr int kXsBudget = 112 * 1024;
+// Largest unit (4 rows of weights) and ring depth.
+constexpr int kUnitMax = 12 * 1024;
+constexpr int kMaxSlots = 24;
+// Chunk values of one CTA at most (bounds its share of rows).
+constexpr int kCvBudget = 32 * 1024;
 
 #if defined(QMV_TUNING)
 // Tuning builds only: fixed launch shapes for sweeps (0 = automatic).
-struct TuneOverride { int whole_k = 0, RB = 0, H = 0, stages = 0, R = 0; };
+struct TuneOverride { int slots = 0, uc = 0, consumers = 0, grid_rows = 0, cpc = 0; };
 TuneOverride g_tune;
 #endif
 
-int pow2_floor(int v)
-{
-    int p = 1;
-    while (p * 2 <= v) p *= 2;
-    return p;
-}
+int xs_bytes(int V, int nsub) { return V == 1 ? nsub * qmv::kXsF32 * 4 : V * nsub * qmv::kXsB16; }
 
-void finish(Problem &pr)
-{
-    pr.tile_rows = pr.RB * pr.RW;
-    pr.smem = qmv::smem_layout(pr.bits, pr.gs, pr.V, pr.RW, pr.warps, pr.stages, pr.gsm, pr.cps, pr.tile_rows).total;
-}
-
-// Launch shape of a call. `sms` is the device's SM count, or 0 when unknown
-// (then no persistent grid is planned). Whether a workspace is needed never
-// depends on `sms`, so qmv_workspace_size can be answered without a GPU.
+// Launch shape of a call. `sms` is the device's SM count, or 0 when unknown.
+// Whether a workspace is needed, and its size, never depend on `sms`, so
+// qmv_workspace_size can be answered without a GPU.
 Problem plan(int V, int N, int K, int bits, int gs, int sms)
 {
-    Problem pr;
-    pr.M = V; pr.V = V; pr.N = N; pr.K = K; pr.bits = bits; pr.gs = gs;
+    Problem pr{};
+    pr.V = V; pr.N = N; pr.K = K; pr.bits = bits; pr.gs = gs;
     pr.G = K / gs;
-    pr.ks = qmv::chunk_count(K, gs);
-    pr.RW = 8;
-    pr.balanced = 0;
-    const int mw = qmv::max_warps(V);
-    int want_whole = -1, want_rb = 0, want_h = 0, want_stages = 0;
+    pr.S_row = qmv::subs_per_row(K);
+    pr.ks = qmv::chunk_count(K);
+    pr.row_bytes = int((long long)K * bits / 8);
+    pr.NB = (N + qmv::kRows - 1) / qmv::kRows;
+    pr.consumers = qmv::consumer_warps(V);
+    pr.threads = 32 * (pr.consumers + qmv::producer_warps(V));
+    // Chunks per CTA: all of K when the staged x of all of K fits, else as many
+    // as fit (one for the streamed kernel).
+    const int per_chunk = xs_bytes(V, qmv::kChunkSubs);
+    if (xs_bytes(V, pr.S_row) <= kXsBudget)
+        pr.cpc = pr.ks;
+    else
+        pr.cpc = V == 1 ? kXsBudget / per_chunk : 1;
 #if defined(QMV_TUNING)
-    if (g_tune.stages >= 2 && g_tune.stages <= 16 && (g_tune.stages & (g_tune.stages - 1)) == 0)
-        want_stages = g_tune.stages;
-    want_whole = g_tune.whole_k ? (g_tune.whole_k > 0 ? 1 : 0) : -1;
-    if (g_tune.whole_k == 2) want_whole = 2;
-    want_rb = g_tune.RB;
-    want_h = g_tune.H;
-    if (V == 1 && (g_tune.R == 2 || g_tune.R == 4)) pr.RW = 4 * g_tune.R;
+    if (g_tune.cpc > 0 && g_tune.cpc <= pr.ks) pr.cpc = g_tune.cpc;
+    if (g_tune.consumers > 0 && g_tune.consumers <= qmv::consumer_warps(V)) {
+        pr.consumers = g_tune.consumers;
+        pr.threads = 32 * (pr.consumers + qmv::producer_warps(V));
+    }
 #endif
-    const int sb = qmv::stage_bytes(bits, gs, pr.RW);
-    pr.stages = want_stages ? want_stages : pow2_floor(8192 / sb > 2 ? 8192 / sb : 2);
-    pr.NB = (N + pr.RW - 1) / pr.RW;
-    // All of K in one CTA (no workspace) when x of all of K fits in shared memory.
-    const bool whole_ok =
-        want_whole != 0 && pr.ks <= qmv::kMaxChunksPerCta &&
-        qmv::smem_layout(bits, gs, V, pr.RW, 1, pr.stages, pr.G, pr.ks, pr.RW).total + 8 * 8192 <= kSmemBudget;
-    if (whole_ok) {
-        pr.cps = pr.ks;
-        pr.gsm = pr.G;
-        // Persistent grid: every SM gets an even share of the row blocks.
-        if (sms > 0 && want_whole != 1 && pr.NB >= sms) {
-            pr.balanced = 1;
-            pr.grid_x = sms;
-            pr.RB = (pr.NB + sms - 1) / sms;
-            pr.H = want_h ? want_h : 1;
-            if (!want_h)
-                while (pr.H < pr.ks && pr.RB * (pr.H + 1) <= mw) ++pr.H;
-            pr.warps = pr.RB * pr.H < mw ? pr.RB * pr.H : mw;
-            finish(pr);
-            while (pr.smem > kSmemBudget && pr.warps > 1) {
-                --pr.warps;
-                finish(pr);
-            }
-            if (pr.smem <= kSmemBudget && pr.H <= pr.cps) {
-                pr.ntiles = pr.grid_x;
-                return pr;
-            }
-            pr.balanced = 0;
-        }
-        pr.H = want_h ? want_h : (pr.ks < mw ? pr.ks : mw);
-        pr.RB = want_rb ? want_rb : (8 / pr.H > 1 ? 8 / pr.H : 1);
-        if (pr.RB * pr.H > mw) pr.RB = mw / pr.H > 0 ? mw / pr.H : 1;
-        if (!want_rb)
-            while (pr.RB > 1 && (pr.NB + pr.RB - 1) / pr.RB < kMinCtas) pr.RB /= 2;
-        pr.warps = pr.RB * pr.H;
-        finish(pr);
-        if (pr.smem <= kSmemBudget && pr.H <= pr.cps && pr.warps <= mw) {
-            pr.ntiles = pr.grid_x = (pr.NB + pr.RB - 1) / pr.RB;
-            return pr;
-        }
+    pr.nranges = (pr.ks + pr.cpc - 1) / pr.cpc;
+    // A persistent grid of about one CTA per SM: the chunk ranges times an
+    // even split of the row blocks.
+    int gr = sms > 0 ? sms / pr.nranges : 1;
+    if (gr < 1) gr = 1;
+    // more CTAs (several waves) when a share of rows would not fit its chunk values
+    const int rb_cap = kCvBudget / (qmv::kRows * pr.cpc * V * 4) > 0 ? kCvBudget / (qmv::kRows * pr.cpc * V * 4) : 1;
+    if ((pr.NB + gr - 1) / gr > rb_cap) gr = (pr.NB + rb_cap - 1) / rb_cap;
+    if (gr > pr.NB) gr = pr.NB;
+#if defined(QMV_TUNING)
+    if (g_tune.grid_rows > 0) gr = g_tune.grid_rows < pr.NB ? g_tune.grid_rows : pr.NB;
+#endif
+    pr.grid_rows = gr;
+    pr.max_rb = (pr.NB + gr - 1) / gr;
+    // Units: whole rows in one contiguous copy when the CTA covers all of K and
+    // four rows are small enough; otherwise uc chunks of each row.
+    const int cb = qmv::chunk_bytes(bits);
+    if (pr.cpc == pr.ks && qmv::kRows * pr.row_bytes <= kUnitMax) {
+        pr.full_rows = 1;
+        pr.uc = pr.ks;
+        pr.pitch = pr.row_bytes;
+    } else {
+        pr.full_rows = 0;
+        pr.uc = kUnitMax / (qmv::kRows * cb);
+        if (pr.uc < 1) pr.uc = 1;
+        if (pr.uc > pr.cpc) pr.uc = pr.cpc;
+#if defined(QMV_TUNING)
+        if (g_tune.uc > 0 && g_tune.uc <= pr.cpc) pr.uc = g_tune.uc;
+#endif
+        pr.pitch = pr.uc * cb;
     }
-    // Otherwise one chunk per CTA; chunk values meet in the workspace.
-    pr.cps = 1;
-    pr.H = 1;
-    pr.gsm = qmv::chunk_groups(gs) < pr.G ? qmv::chunk_groups(gs) : pr.G;
-    pr.RB = want_rb ? (want_rb < mw ? want_rb : mw) : (8 < mw ? 8 : mw);
-    if (!want_rb)
-        while (pr.RB > 1 && (pr.NB + pr.RB - 1) / pr.RB * pr.ks < kMinCtas) pr.RB /= 2;
-    pr.warps = pr.RB;
-    finish(pr);
-    while (pr.smem > kSmemBudget && pr.stages > 2) {
-        pr.stages /= 2;
-        finish(pr);
+    // Scale/bias boxes: one per unit when the four rows' groups fit one box,
+    // else one per row. A box starts at a multiple of 8 elements, so it spans
+    // up to 7 more.
+    const int gpu = pr.full_rows ? pr.G : (pr.uc * qmv::kChunkElems / gs < pr.G ? pr.uc * qmv::kChunkElems / gs : pr.G);
+    if (pr.full_rows && qmv::kRows * pr.G + 7 <= 256) {
+        pr.sb_mode_unit = 1;
+        pr.sbox = qmv::align_up(qmv::kRows * pr.G + 7, 8);
+    } else {
+        pr.sb_mode_unit = 0;
+        pr.sbox = qmv::align_up(gpu + 7, 8);
     }
-    pr.ntiles = pr.grid_x = (pr.NB + pr.RB - 1) / pr.RB;
+    const int nsub = pr.cpc * qmv::kChunkSubs < pr.S_row ? pr.cpc * qmv::kChunkSubs : pr.S_row;
+    auto layout = [&](int slots) {
+        return qmv::smem_layout(bits, V, pr.pitch, pr.sb_mode_unit, pr.sbox, slots, nsub, pr.max_rb, pr.cpc);
+    };
+    // Ring depth: as many slots as fit, but no more than the units of a CTA.
+    const int upr = (pr.cpc + pr.uc - 1) / pr.uc;
+    const int units = pr.max_rb * upr;
+    int slots = kMaxSlots < units ? kMaxSlots : units;
+    if (slots < 2) slots = 2;
+#if defined(QMV_TUNING)
+    if (g_tune.slots >= 2) slots = g_tune.slots;
+#endif
+    // every slot is served by one producer: a multiple of the producer count
+    const int P = qmv::producer_warps(V);
+    slots = (slots + P - 1) / P * P;
+    while (slots > P && layout(slots).total > kSmemBudget) slots -= P;
+    pr.slots = slots;
+    pr.smem = layout(slots).total;
+    // A consumer waits on a slot's "full" barrier by phase parity, which is
+    // only unambiguous while no consumer can run two laps of the ring ahead of
+    // the producer: at most one consumer warp per slot.
+    if (pr.consumers > pr.slots) {
+        pr.consumers = pr.slots;
+        pr.threads = 32 * (pr.consumers + P);
+    }
     return pr;
 }
 
-size_t counter_bytes(int ntiles) { return (size_t(ntiles) * sizeof(unsigned) + 255) & ~size_t(255); }
+size_t counter_bytes(int NB) { return (size_t(NB) * sizeof(unsigned) + 255) & ~size_t(255); }
 
 size_t workspace_bytes_for(const Problem &pr)
 {
-    if (pr.cps == pr.ks) return 0;
-    return counter_bytes(pr.ntiles) + size_t(pr.ks) * size_t(pr.V) * size_t(pr.N) * sizeof(float);
+    if (pr.cpc >= pr.ks) return 0;
+    return counter_bytes(pr.NB) + size_t(pr.ks) * size_t(pr.V) * size_t(pr.N) * sizeof(float);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
@@ -197,19 +211,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// Weight matrix as a 2-D byte tensor [N rows, K*bits/8 bytes]; one box is
-// 128 bytes x (rows per block), 128B-swizzled in shared memory.
-int encode_weight_map(CUtensorMap *map, const uint32_t *w_q, const Problem &pr)
+// Scales or biases as a 1-D bf16 tensor of N*G elements; one box is `sbox`
+// elements. Elements past the end arrive as zeros.
+int encode_sb_map(CUtensorMap *map, const uint16_t *base, const Problem &pr)
 {
     auto fn = encode_fn();
     if (!fn) return -1;
-    const cuuint64_t row_bytes = cuuint64_t(pr.K) * pr.bits / 8;
-    const cuuint64_t dims[2] = {row_bytes, cuuint64_t(pr.N)};
-    const cuuint64_t strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {cuuint32_t(qmv::kBoxBytes), cuuint32_t(pr.RW)};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint32_t *>(w_q), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const cuuint64_t dims[1] = {cuuint64_t(pr.N) * cuuint64_t(pr.G)};
+    const cuuint64_t strides[1] = {0};
+    const cuuint32_t box[1] = {cuuint32_t(pr.sbox)};
+    const cuuint32_t estr[1] = {1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 1, const_cast<uint16_t *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return int(r);
 }
@@ -267,16 +280,18 @@ qmv_status library_workspace(int dev, size_t need, void **out)
     return QMV_OK;
 }
 
-cudaError_t dispatch(const Problem &pr, const CUtensorMap &map, const qmv::Params &p, cudaStream_t stream)
+cudaError_t dispatch(const Problem &pr, const CUtensorMap &map_s, const CUtensorMap &map_b, const qmv::Params &p,
+                     bool pdl, cudaStream_t stream)
 {
-    const dim3 grid(pr.grid_x, pr.ks / pr.cps);
-    const int threads = 32 * pr.warps;
-    const size_t smem = size_t(pr.smem);
-    const int R = pr.RW / 4;
-    if (pr.bits == 4 && pr.gs == 64) return qmv::launch_b4g64(pr.V, R, map, p, grid, threads, smem, stream);
-    if (pr.bits == 4 && pr.gs == 128) return qmv::launch_b4g128(pr.V, R, map, p, grid, threads, smem, stream);
-    if (pr.bits == 2 && pr.gs == 64) return qmv::launch_b2g64(pr.V, R, map, p, grid, threads, smem, stream);
-    return qmv::launch_b2g128(pr.V, R, map, p, grid, threads, smem, stream);
+    qmv::Launch l;
+    l.grid = dim3(pr.grid_rows, pr.nranges);
+    l.threads = pr.threads;
+    l.smem = size_t(pr.smem);
+    l.pdl = pdl;
+    if (pr.bits == 4 && pr.gs == 64) return qmv::launch_b4g64(pr.V, map_s, map_b, p, l, stream);
+    if (pr.bits == 4 && pr.gs == 128) return qmv::launch_b4g128(pr.V, map_s, map_b, p, l, stream);
+    if (pr.bits == 2 && pr.gs == 64) return qmv::launch_b2g64(pr.V, map_s, map_b, p, l, stream);
+    return qmv::launch_b2g128(pr.V, map_s, map_b, p, l, stream);
 }
 
 qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t *biases, const uint16_t *x, void *y,
@@ -286,9 +301,9 @@ qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t 
     if (!w_q || !scales || !biases || !x || !y) return QMV_ERR_NULL;
     qmv_status st = check_shape(M, N, K, bits, gs, true);
     if (st != QMV_OK) return st;
-    if (flags & ~(QMV_F32_OUT | QMV_FORCE_M1_PER_COLUMN)) return QMV_ERR_FLAGS;
+    if (flags & ~(QMV_F32_OUT | QMV_FORCE_M1_PER_COLUMN | QMV_PDL)) return QMV_ERR_FLAGS;
     const bool f32_out = (flags & QMV_F32_OUT) != 0;
-    if (!aligned(w_q, 16) || !aligned(x, 16) || !aligned(scales, 2) || !aligned(biases, 2) ||
+    if (!aligned(w_q, 16) || !aligned(x, 16) || !aligned(scales, 16) || !aligned(biases, 16) ||
         !aligned(y, f32_out ? 4 : 2) || (workspace && !aligned(workspace, 16)))
         return QMV_ERR_ALIGN;
 
@@ -303,6 +318,10 @@ qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t 
     st = sm_count(dev, &sms);
     if (st != QMV_OK) return st;
     const Problem pr = plan(V, N, K, bits, gs, sms);
+    if (pr.smem > kSmemBudget) {  // only a tuning override can get here
+        snprintf(g_last_error, sizeof g_last_error, "launch plan needs %d bytes of shared memory", pr.smem);
+        return QMV_ERR_CUDA;
+    }
     const size_t need = workspace_bytes_for(pr);
     if (need > 0) {
         if (workspace) {
@@ -316,31 +335,33 @@ qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t 
     st = device_error_ptr(dev, &err);
     if (st != QMV_OK) return st;
 
-    CUtensorMap map;
-    const int enc = encode_weight_map(&map, w_q, pr);
+    CUtensorMap map_s, map_b;
+    int enc = encode_sb_map(&map_s, scales, pr);
+    if (enc == 0) enc = encode_sb_map(&map_b, biases, pr);
     if (enc != 0) {
-        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled(weights) returned %d%s", enc,
+        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled(scales/biases) returned %d%s", enc,
                  enc < 0 ? " (driver entry point not found)" : "");
         return QMV_ERR_CUDA;
     }
 
     qmv::Params p;
-    p.scales = scales;
-    p.biases = biases;
+    p.w = reinterpret_cast<const uint8_t *>(w_q);
     p.err = err;
-    p.N = N; p.K = K; p.G = pr.G; p.ks = pr.ks; p.cps = pr.cps; p.RB = pr.RB; p.H = pr.H;
-    p.warps = pr.warps; p.NB = pr.NB; p.balanced = pr.balanced;
-    p.stages = pr.stages; p.gsm = pr.gsm; p.ntiles = pr.ntiles;
+    p.N = N; p.K = K; p.G = pr.G; p.S_row = pr.S_row; p.ks = pr.ks; p.row_bytes = pr.row_bytes;
+    p.NB = pr.NB; p.grid_rows = pr.grid_rows; p.cpc = pr.cpc; p.uc = pr.uc; p.full_rows = pr.full_rows;
+    p.pitch = pr.pitch; p.sb_mode_unit = pr.sb_mode_unit; p.sbox = pr.sbox; p.slots = pr.slots;
+    p.consumers = pr.consumers; p.max_rb = pr.max_rb;
     p.f32_out = f32_out ? 1 : 0;
     p.counters = need ? static_cast<unsigned *>(workspace) : nullptr;
-    p.partials = need ? reinterpret_cast<float *>(static_cast<char *>(workspace) + counter_bytes(pr.ntiles)) : nullptr;
+    p.partials = need ? reinterpret_cast<float *>(static_cast<char *>(workspace) + counter_bytes(pr.NB)) : nullptr;
 
+    const bool pdl = (flags & QMV_PDL) != 0;
     const size_t ysize = f32_out ? sizeof(float) : sizeof(uint16_t);
     const int launches = per_column ? M : 1;
     for (int m = 0; m < launches; ++m) {
         p.x = x + size_t(m) * K;
         p.y = static_cast<char *>(y) + size_t(m) * N * ysize;
-        ce = dispatch(pr, map, p, stream);
+        ce = dispatch(pr, map_s, map_b, p, pdl, stream);
         if (ce != cudaSuccess) return cuda_fail("kernel launch", ce);
     }
     return QMV_OK;
@@ -351,17 +372,18 @@ qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t 
 extern "C" int qmv_split_count(int N, int K, int bits, int group_size)
 {
     if (check_shape(1, N, K, bits, group_size, false) != QMV_OK) return 0;
-    return qmv::chunk_count(K, group_size);
+    return qmv::chunk_count(K);
 }
 
 #if defined(QMV_TUNING)
-extern "C" __attribute__((visibility("default"))) void qmv_tune_set(int whole_k, int RB, int H, int stages, int R)
+extern "C" __attribute__((visibility("default"))) void qmv_tune_set(int slots, int uc, int consumers, int grid_rows,
+                                                                     int cpc)
 {
-    g_tune.whole_k = whole_k;
-    g_tune.RB = RB;
-    g_tune.H = H;
-    g_tune.stages = stages;
-    g_tune.R = R;
+    g_tune.slots = slots;
+    g_tune.uc = uc;
+    g_tune.consumers = consumers;
+    g_tune.grid_rows = grid_rows;
+    g_tune.cpc = cpc;
 }
 #endif
 
@@ -420,7 +442,7 @@ extern "C" const char *qmv_status_string(qmv_status s)
         case QMV_ERR_GROUP: return "QMV_ERR_GROUP: group_size must be 64 or 128";
         case QMV_ERR_SHAPE: return "QMV_ERR_SHAPE: need 1 <= N <= 2^30, 1 <= K <= 2^24, K % group_size == 0";
         case QMV_ERR_M_RANGE: return "QMV_ERR_M_RANGE: M must be in [1, 16]";
-        case QMV_ERR_ALIGN: return "QMV_ERR_ALIGN: w_q, x and workspace need 16-byte alignment, scales/biases/y 2 (f32 y: 4)";
+        case QMV_ERR_ALIGN: return "QMV_ERR_ALIGN: w_q, x, scales, biases and workspace need 16-byte alignment, y 2 (f32 y: 4)";
         case QMV_ERR_CUDA: return "QMV_ERR_CUDA: a CUDA runtime call or kernel launch failed";
         case QMV_ERR_WORKSPACE: return "QMV_ERR_WORKSPACE: workspace smaller than qmv_workspace_size()";
         case QMV_ERR_VALUE: return "QMV_ERR_VALUE: a quantized value does not fit in `bits` bits";

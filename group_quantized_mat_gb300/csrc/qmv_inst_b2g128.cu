@@ -2,9 +2,9 @@
 #include "qmv_launch.cuh"
 
 namespace qmv {
-cudaError_t launch_b2g128(int V, int R, const CUtensorMap &map, const Params &p, dim3 grid, int threads,
-                          size_t smem, cudaStream_t stream)
+cudaError_t launch_b2g128(int V, const CUtensorMap &map_s, const CUtensorMap &map_b, const Params &p, const Launch &l,
+                         cudaStream_t stream)
 {
-    return launch_bits_gs<2, 128>(V, R, map, p, grid, threads, smem, stream);
+    return launch_bits_gs<2, 128>(V, map_s, map_b, p, l, stream);
 }
 }  // namespace qmv

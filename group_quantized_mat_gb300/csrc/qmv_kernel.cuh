@@ -1,38 +1,44 @@
-// sm_103a kernels of the affine group-quantized mat-vec:
+// sm_103a kernel of the affine group-quantized mat-vec:
 //
 //   y[m, n] = sum_g ( s[n,g] * sum_{i in g} q[n,i] x[m,i] + b[n,g] * sum_{i in g} x[m,i] )
 //
-// the factored group dot of mlxcel issue #1289 ("Correction to the obvious
-// sketch": scale * accum + sum * bias, no dequantized weight) applied once per
-// group (mlxcel PR #1681, "Not covered"), and its order-preserving streamed
-// form (#1289 "Step 2"): the weights are read and decoded once and reused for
-// V <= 16 activation vectors, each vector's fp32 operation sequence being
-// exactly the one an M = 1 launch performs.
+// evaluated in the factored form of mlxcel issue #1289 ("Correction to the
+// obvious sketch": scale * accum + sum * bias, no dequantized weight) and
+// streamed for V <= 16 activation vectors from one read of the weights
+// (#1289 "Step 2"), each vector's fp32 operation sequence being exactly the one
+// a V = 1 launch performs.
 //
-// Work decomposition (none of it changes the arithmetic):
-//  * a row block is 4R consecutive rows; in the warp processing it, lane
-//    (p, j), p = lane/8, j = lane%8, owns rows {p, p+4, ..., p+4(R-1)} and
-//    slice j of every stage;
-//  * a stage is 8 consecutive groups of the row block, one per slice, brought
-//    into a private ring of the warp by 2-D TMA boxes (128 bytes x 4R rows,
-//    128B-swizzled), one mbarrier per ring slot; lane 0 refills a slot once the
-//    warp has read it;
-//  * a CTA owns row blocks and a range of K-chunks (see Params); x of its chunk
-//    range is staged once into shared memory as fp32, each value
-//    pre-multiplied by 2^(-bits * k) (k = its field position inside a 16-bit
-//    half word) and padded by 16 bytes per group, so the eight slices hit eight
-//    different bank groups; sum(x) per group is staged beside it.
-//
-// Fixed fp32 order of output (m, n), for every M:
-//  1. group: two running sums over even and odd elements, each in increasing
-//     order from +0 (one packed fma.rn.f32x2 per element pair): d = a_e + a_o.
-//     Every product q*x is exact in fp32 (small integer times 8-bit mantissa);
-//  2. fold: P = fma(s_g, d, P); P = fma(b_g, sx_g, P), sx_g = eight sums of
-//     eight consecutive x (each left to right) added left to right; P of
-//     slice j runs over groups j, j+8, ... of the chunk in increasing order;
-//  3. chunk value = butterfly over the eight slices (xor 4, 2, 1);
-//  4. y = ((c_0 + c_1) + c_2) + ... over the chunks of kChunkElems elements;
+// Fixed fp32 order of output (m, n), the same for every V:
+//  1. subgroup t (64 consecutive elements of row n, inside one quantization
+//     group g): with E the largest exponent field among its 64 bf16 x values
+//     (at least 1), each x_i is staged as x'_i = x_i * 2^(254 - bits*k_i - E)
+//     (k_i = position of element i inside its 16-bit half word), exactly a
+//     bf16 value, and each field q_i is read as the fp32 whose bit pattern is
+//     q_i << (bits*k_i) -- the subnormal q_i * 2^(bits*k_i - 149) -- so every
+//     product equals q_i * x_i * 2^(105 - E) exactly (for all x_i down to
+//     2^-120 times the subgroup's largest). Two running sums a_e, a_o over the
+//     even and odd elements, in processing order from +0, one packed
+//     fma.rn.f32x2 per element pair; d = ((a_e + a_o) * f1) * f2 with
+//     f1 * f2 = 2^(E - 105);
+//  2. term = fma(s_g, d, b_g * sx), sx = sum of the subgroup's 64 x: eight
+//     sums of eight consecutive elements (each left to right) added left to
+//     right;
+//  3. chunk value (32 subgroups, 2048 elements; lanes past the row's end add
+//     +0) = binary tree over the 32 subgroup slots l: pairs (l, l^16) first,
+//     then (l, l^8), (l, l^4), (l, l^2), (l, l^1);
+//  4. y = ((c_0 + c_1) + c_2) + ... over the chunks of the row;
 //  5. one rounding to bf16, nearest even.
+// Processing order inside a 4-bit subgroup: its two 16-byte halves, the half
+// selected by bit 2 of the subgroup index first (that keeps the eight lanes of
+// a shared-memory phase on distinct banks); inside a half, increasing element
+// order. 2-bit subgroups run in increasing element order.
+//
+// Work decomposition (none of it changes the arithmetic): a unit is 4 rows x
+// uc chunks; lane l of the warp processing a unit owns subgroup l of each of
+// its chunks in all 4 rows. One producer warp streams units into a ring of
+// shared-memory slots (1-D bulk copies of the weight rows, 1-D tensor-map boxes
+// of scales and biases, one mbarrier per slot for "full" and one for "empty");
+// consumer warps take units in order from a shared counter.
 #pragma once
 
 #include <cuda.h>
@@ -62,9 +68,9 @@ __device__ __forceinline__ void fence_mbar_init()
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem()
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
 {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
@@ -108,6 +114,25 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     return false;
 }
 
+// Bounded wait until a producer's issued-unit count passes unit u.
+__device__ __forceinline__ bool wait_issued(volatile int *count, int u)
+{
+    if (*count > u) {
+        __threadfence_block();
+        return true;
+    }
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0; it < (1u << 24); ++it) {
+        __nanosleep(32);
+        if (*count > u) {
+            __threadfence_block();
+            return true;
+        }
+        if (global_timer_ns() - t0 > 2000000000ull) return false;
+    }
+    return false;
+}
+
 __device__ __forceinline__ uint64_t l2_evict_first_policy()
 {
     uint64_t pol;
@@ -115,85 +140,36 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy()
     return pol;
 }
 
-// 2-D TMA tile load (global -> this CTA's shared memory), completion counted
-// in bytes on `bar`. x is the byte column, y the row.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            uint32_t bar, uint64_t policy)
+// 1-D bulk copy global -> this CTA's shared memory (16-byte aligned addresses,
+// size a multiple of 16), completion counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy)
 {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
         : "memory");
 }
 
-__device__ __forceinline__ float bf16_bits_to_f32(uint16_t h)
+// 1-D tensor-map box load at element coordinate x (a multiple of 8 for
+// 2-byte elements); elements past the tensor's end arrive as zeros.
+__device__ __forceinline__ void tma_load_1d(uint32_t dst, const CUtensorMap *map, int x, uint32_t bar)
 {
-    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+    asm volatile(
+        "cp.async.bulk.tensor.1d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2}], [%3];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(bar)
+        : "memory");
 }
 
-// ------------------------------------------------------ field extraction --
+// Programmatic dependent launch: wait until the preceding grid on the stream
+// has completed and its memory is visible (returns at once when the launch had
+// no programmatic dependency), and allow the next grid to be scheduled.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
-// binary32 2^23: OR-ing an integer m < 2^23 into its significand gives 2^23 + m.
-constexpr uint32_t kMagic = 0x4B000000u;
-
-// Pairs of fp32 values travel as one 64-bit register (low half = first
-// element), the operand form of the packed f32x2 instructions.
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c)
-{
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-
-__device__ __forceinline__ float pair_lo(uint64_t v) { return __uint_as_float(uint32_t(v)); }
-__device__ __forceinline__ float pair_hi(uint64_t v) { return __uint_as_float(uint32_t(v >> 32)); }
-
-// Elements of a packed word at masks MASK_LO and MASK_HI, as the exact pair
-// (q_lo * 2^(bits*k_lo), q_hi * 2^(bits*k_hi)): each field is OR-ed into the
-// significand of 2^23 (one LOP3 each, the mask as immediate, the magic
-// constant in a register) and 2^23 is subtracted from both halves at once.
-template <uint32_t MASK_LO, uint32_t MASK_HI>
-__device__ __forceinline__ uint64_t field_pair(uint32_t w, uint32_t magic, uint64_t neg_magic2)
-{
-    uint64_t d;
-    asm("{\n\t.reg .b32 lo, hi;\n\t.reg .b64 t;\n\t"
-        "lop3.b32 lo, %1, %2, %4, 0xEA;\n\t"
-        "lop3.b32 hi, %1, %3, %4, 0xEA;\n\t"
-        "mov.b64 t, {lo, hi};\n\t"
-        "add.rn.f32x2 %0, t, %5;\n\t}"
-        : "=l"(d)
-        : "r"(w), "n"(MASK_LO), "n"(MASK_HI), "r"(magic), "l"(neg_magic2));
-    return d;
-}
-
-// Element pairs (2p, 2p+1) of one packed word, as exact floats q * 2^(bits*k),
-// k the element's position inside its 16-bit half. The matching x values were
-// staged pre-multiplied by 2^(-bits*k), so each product equals q * x exactly.
-template <int BITS>
-__device__ __forceinline__ void extract_pairs(uint32_t w, uint32_t magic, uint64_t nm, uint64_t (&q)[16 / BITS])
-{
-    // w >> 16 as a multiply-high, which runs on the FMA pipe (the extraction
-    // keeps the integer/logic pipe busy).
-    uint32_t hi;
-    asm("mul.hi.u32 %0, %1, 65536;" : "=r"(hi) : "r"(w));
-    const uint32_t lo = w;
-    if constexpr (BITS == 4) {
-        q[0] = field_pair<0x000Fu, 0x00F0u>(lo, magic, nm);
-        q[1] = field_pair<0x0F00u, 0xF000u>(lo, magic, nm);
-        q[2] = field_pair<0x000Fu, 0x00F0u>(hi, magic, nm);
-        q[3] = field_pair<0x0F00u, 0xF000u>(hi, magic, nm);
-    } else {
-        q[0] = field_pair<0x0003u, 0x000Cu>(lo, magic, nm);
-        q[1] = field_pair<0x0030u, 0x00C0u>(lo, magic, nm);
-        q[2] = field_pair<0x0300u, 0x0C00u>(lo, magic, nm);
-        q[3] = field_pair<0x3000u, 0xC000u>(lo, magic, nm);
-        q[4] = field_pair<0x0003u, 0x000Cu>(hi, magic, nm);
-        q[5] = field_pair<0x0030u, 0x00C0u>(hi, magic, nm);
-        q[6] = field_pair<0x0300u, 0x0C00u>(hi, magic, nm);
-        q[7] = field_pair<0x3000u, 0xC000u>(hi, magic, nm);
-    }
-}
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
 
 __device__ __forceinline__ void lds_v2_u64(uint32_t addr, uint64_t &a, uint64_t &b)
 {
@@ -207,333 +183,576 @@ __device__ __forceinline__ uint4 lds_v4_u32(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ float4 lds_f4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr)
+{
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+
+// ------------------------------------------------------- the datapath --
+
+// Pairs of fp32 values travel as one 64-bit register (low half = first
+// element), the operand form of the packed f32x2 instructions.
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi)
+{
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
+}
+
+__device__ __forceinline__ float pair_lo(uint64_t v) { return __uint_as_float(uint32_t(v)); }
+__device__ __forceinline__ float pair_hi(uint64_t v) { return __uint_as_float(uint32_t(v >> 32)); }
+
+// w >> 16 as a multiply-high, which runs on the FMA pipe (the field masks keep
+// the integer/logic pipe busy).
+__device__ __forceinline__ uint32_t hi_half(uint32_t w)
+{
+    uint32_t h;
+    asm("mul.hi.u32 %0, %1, 65536;" : "=r"(h) : "r"(w));
+    return h;
+}
+
+// The four element pairs of an octet (8 consecutive elements in processing
+// order) as fp32 bit patterns q << (bits*k): one mask per element.
+//   4-bit: the octet is one word; pairs (0,1), (2,3) from its low half and
+//          (4,5), (6,7) from its high half `h`.
+//   2-bit: the octet is one 16-bit half `u` of a word.
+__device__ __forceinline__ void octet_pairs4(uint32_t w, uint32_t h, uint64_t (&q)[4])
+{
+    q[0] = pack2(w & 0x000Fu, w & 0x00F0u);
+    q[1] = pack2(w & 0x0F00u, w & 0xF000u);
+    q[2] = pack2(h & 0x000Fu, h & 0x00F0u);
+    q[3] = pack2(h & 0x0F00u, h & 0xF000u);
+}
+
+__device__ __forceinline__ void octet_pairs2(uint32_t u, uint64_t (&q)[4])
+{
+    q[0] = pack2(u & 0x0003u, u & 0x000Cu);
+    q[1] = pack2(u & 0x0030u, u & 0x00C0u);
+    q[2] = pack2(u & 0x0300u, u & 0x0C00u);
+    q[3] = pack2(u & 0x3000u, u & 0xC000u);
+}
+
 __device__ __forceinline__ uint32_t word_of(const uint4 &c, int k)
 {
     return k == 0 ? c.x : (k == 1 ? c.y : (k == 2 ? c.z : c.w));
 }
 
-// ----------------------------------------------------------- group dot --
-
-// Step 1 of the fixed order for one group of the lane's R rows against V
-// staged vectors: acc[r][v] = (a_e, a_o) as one 64-bit pair.
-//   box     shared address of the stage;
-//   woff[r] byte offset in the stage of the first 16-byte chunk of slice j's
-//           group in row pr + 4r (128B swizzle applied; chunk c of the group
-//           sits at woff ^ (c << 4));
-//   xg      shared address of the group's staged x (vector 0); xvstride in bytes.
-template <int BITS, int GS, int V, int R>
-__device__ __forceinline__ void group_dot(uint32_t box, const uint32_t (&woff)[R], uint32_t xg, uint32_t xvstride,
-                                          uint32_t magic, uint64_t nm, uint64_t (&acc)[R][V])
+// Pairs of octet `o` (0..7 in processing order) of a subgroup, for BITS.
+// quads[p] = the subgroup's p-th 16-byte piece as loaded (4-bit: two pieces,
+// processing order; 2-bit: one piece).
+template <int BITS>
+__device__ __forceinline__ void subgroup_octet(const uint4 (&quads)[BITS == 4 ? 2 : 1], int o, uint64_t (&q)[4])
 {
-    constexpr int kChunks = group_bytes(BITS, GS) / 16;
-    constexpr int kPerWord = 32 / BITS;
+    if constexpr (BITS == 4) {
+        const uint32_t w = word_of(quads[o >> 2], o & 3);
+        octet_pairs4(w, hi_half(w), q);
+    } else {
+        const uint32_t w = word_of(quads[0], o >> 1);
+        octet_pairs2((o & 1) ? hi_half(w) : w, q);
+    }
+}
 
-    uint4 w[R][kChunks];
+// Byte offsets, inside one row of a slot, of the lane's subgroup pieces in
+// processing order (4-bit: the half selected by bit 2 of the subgroup first).
+template <int BITS>
+__device__ __forceinline__ void piece_offsets(int lane, uint32_t (&off)[BITS == 4 ? 2 : 1])
+{
+    if constexpr (BITS == 4) {
+        const uint32_t first = ((lane >> 2) & 1) * 16u;
+        off[0] = uint32_t(lane) * 32u + first;
+        off[1] = uint32_t(lane) * 32u + (16u - first);
+    } else {
+        off[0] = uint32_t(lane) * 16u;
+    }
+}
+
+// Step 1 for V = 1: acc[r] = (a_e, a_o) of the lane's subgroup in rows 0..3.
+//   wrow[r]  shared address of row r's subgroup bytes (piece offsets added);
+//   xsub     shared address of the staged subgroup (64 fp32 x' in processing order).
+template <int BITS>
+__device__ __forceinline__ void subgroup_dot_v1(const uint32_t (&wrow)[kRows][BITS == 4 ? 2 : 1], uint32_t xsub,
+                                                uint64_t (&acc)[kRows])
+{
+    constexpr int NP = BITS == 4 ? 2 : 1;
+    uint4 quads[kRows][NP];
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+    for (int r = 0; r < kRows; ++r)
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c) w[r][c] = lds_v4_u32(box + (woff[r] ^ (c << 4)));
+        for (int pc = 0; pc < NP; ++pc) quads[r][pc] = lds_v4_u32(wrow[r][pc]);
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+    for (int r = 0; r < kRows; ++r) acc[r] = 0ull;
 #pragma unroll
-        for (int v = 0; v < V; ++v) acc[r][v] = 0ull;
+    for (int o = 0; o < 8; ++o) {
+        uint64_t x01, x23, x45, x67;
+        lds_v2_u64(xsub + o * 32, x01, x23);
+        lds_v2_u64(xsub + o * 32 + 16, x45, x67);
 #pragma unroll
-    for (int wi = 0; wi < kChunks * 4; ++wi) {
-        uint64_t q[R][kPerWord / 2];
+        for (int r = 0; r < kRows; ++r) {
+            uint64_t q[4];
+            subgroup_octet<BITS>(quads[r], o, q);
+            acc[r] = ffma2(q[0], x01, acc[r]);
+            acc[r] = ffma2(q[1], x23, acc[r]);
+            acc[r] = ffma2(q[2], x45, acc[r]);
+            acc[r] = ffma2(q[3], x67, acc[r]);
+        }
+    }
+}
+
+// Step 1 for VP vectors from bf16-staged x': acc[r][v].
+//   xsub   shared address of vector 0's staged subgroup; xv bytes between vectors.
+template <int BITS, int VP>
+__device__ __forceinline__ void subgroup_dot_vp(const uint32_t (&wrow)[kRows][BITS == 4 ? 2 : 1], uint32_t xsub,
+                                                uint32_t xv, uint64_t (&acc)[kRows][VP])
+{
+    constexpr int NP = BITS == 4 ? 2 : 1;
+    uint4 quads[kRows][NP];
 #pragma unroll
-        for (int r = 0; r < R; ++r) extract_pairs<BITS>(word_of(w[r][wi / 4], wi % 4), magic, nm, q[r]);
+    for (int r = 0; r < kRows; ++r)
 #pragma unroll
-        for (int v = 0; v < V; ++v) {
+        for (int pc = 0; pc < NP; ++pc) quads[r][pc] = lds_v4_u32(wrow[r][pc]);
 #pragma unroll
-            for (int hh = 0; hh < kPerWord / 4; ++hh) {
-                uint64_t x01, x23;
-                lds_v2_u64(xg + v * xvstride + (wi * kPerWord + hh * 4) * 4, x01, x23);
+    for (int r = 0; r < kRows; ++r)
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    acc[r][v] = ffma2(q[r][2 * hh], x01, acc[r][v]);
-                    acc[r][v] = ffma2(q[r][2 * hh + 1], x23, acc[r][v]);
-                }
+        for (int v = 0; v < VP; ++v) acc[r][v] = 0ull;
+#pragma unroll
+    for (int o = 0; o < 8; ++o) {
+        uint64_t q[kRows][4];
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) subgroup_octet<BITS>(quads[r], o, q[r]);
+#pragma unroll
+        for (int v = 0; v < VP; ++v) {
+            const uint4 xb = lds_v4_u32(xsub + v * xv + o * 16);
+            const uint64_t x01 = pack2(xb.x << 16, xb.x & 0xFFFF0000u);
+            const uint64_t x23 = pack2(xb.y << 16, xb.y & 0xFFFF0000u);
+            const uint64_t x45 = pack2(xb.z << 16, xb.z & 0xFFFF0000u);
+            const uint64_t x67 = pack2(xb.w << 16, xb.w & 0xFFFF0000u);
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) {
+                acc[r][v] = ffma2(q[r][0], x01, acc[r][v]);
+                acc[r][v] = ffma2(q[r][1], x23, acc[r][v]);
+                acc[r][v] = ffma2(q[r][2], x45, acc[r][v]);
+                acc[r][v] = ffma2(q[r][3], x67, acc[r][v]);
             }
         }
     }
 }
 
+// Step 2: the subgroup's term from its pair sums.
+template <bool STREAMED>
+__device__ __forceinline__ float subgroup_term(uint64_t acc, float s, float b, float sx, float f1, float f2)
+{
+    float d = __fadd_rn(pair_lo(acc), pair_hi(acc));
+    d = __fmul_rn(__fmul_rn(d, f1), f2);
+#if defined(QMV_TEST_MUTATE_ORDER)
+    // Test-only build: the streamed kernel adds the bias term last instead, a
+    // different fp32 order that the bit-identity tests must be able to detect.
+    if constexpr (STREAMED) return __fadd_rn(__fmul_rn(s, d), __fmul_rn(b, sx));
+#endif
+    return __fmaf_rn(s, d, __fmul_rn(b, sx));
+}
+
+// Step 3 for N values per lane (N a power of two, at most 32): the binary
+// tree over the 32 lanes, as a reduce-scatter. At the step with mask m a lane
+// keeps half of its values (the upper half if lane & m) and adds its
+// partner's copy of them, so every partial sum is exactly the tree's. After
+// log2(N) steps lane l holds value index l >> (5 - log2 N); the remaining
+// steps are plain butterflies. Returns that value (the full 32-lane sum).
+template <int N>
+__device__ __forceinline__ float tree_reduce_scatter(float (&val)[N], int lane)
+{
+    constexpr int LOG = N == 1 ? 0 : N == 2 ? 1 : N == 4 ? 2 : N == 8 ? 3 : N == 16 ? 4 : 5;
+    static_assert((1 << LOG) == N, "N must be a power of two <= 32");
+#pragma unroll
+    for (int step = 0; step < LOG; ++step) {
+        const int m = 16 >> step;
+        const int half = N >> (step + 1);
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float keep = upper ? val[half + i] : val[i];
+            const float send = upper ? val[i] : val[half + i];
+            val[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, m));
+        }
+    }
+    float t = val[0];
+#pragma unroll
+    for (int step = LOG; step < 5; ++step) t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 16 >> step));
+    return t;
+}
+
+__device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
 // ---------------------------------------------------------------- kernel --
 
-template <int BITS, int GS, int V, int R>
-__device__ __forceinline__ void qmv_body(const CUtensorMap *tmap_w, const Params &p)
-{
-    constexpr int RW = 4 * R;  // rows per row block (one warp's rows)
-    constexpr int kGB = group_bytes(BITS, GS);
-    constexpr int kGPB = groups_per_box(BITS, GS);
-    constexpr int kBPS = boxes_per_stage(BITS, GS);
-    constexpr int kCG = chunk_groups(GS);
-    constexpr int kSPC = kCG / kSlices;  // stages per full chunk (4 or 2)
-    constexpr int kXS = x_stride(GS);
-    constexpr int kPerHalf = 16 / BITS;
-    constexpr int kBoxSmem = kBoxBytes * RW;
-    constexpr int kStageBytes = kBPS * kBoxSmem;
+template <int BITS, int V>
+struct Traits {
+    static constexpr int VP = V <= 8 ? V : (V + 1) / 2;       // vectors per pass
+    static constexpr int PASSES = (V + VP - 1) / VP;
+    static constexpr int NVAL = kRows * VP;
+    static constexpr int NRED = NVAL <= 4 ? 4 : NVAL <= 8 ? 8 : NVAL <= 16 ? 16 : 32;
+    static constexpr int NP = BITS == 4 ? 2 : 1;              // 16-byte pieces per subgroup row
+};
 
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
+template <int BITS, int GS, int V>
+__device__ __forceinline__ void qmv_body(const CUtensorMap *map_s, const CUtensorMap *map_b, const Params &p)
+{
+    using T = Traits<BITS, V>;
+    constexpr int kSubB = sub_bytes(BITS);
+    constexpr int kChunkB = chunk_bytes(BITS);
+
+    extern __shared__ __align__(128) uint8_t smem_raw[];
     __shared__ unsigned s_ticket;
-    // Align the dynamic base to 1024 bytes (the 128B swizzle pattern repeats
-    // every 1024 bytes) by offsetting the __shared__ array itself, so every
-    // access below stays a shared-memory access.
-    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const int nwarps = p.warps;
-    const int nthreads = nwarps * 32;
-    const int tile_rows = p.RB * RW;  // rows the CTA's chunk-value buffer holds
-    const SmemLayout L = smem_layout(BITS, GS, V, RW, nwarps, p.stages, p.gsm, p.cps, tile_rows);
-    float *xs = reinterpret_cast<float *>(smem + L.xs);
-    float *sxs = reinterpret_cast<float *>(smem + L.sx);
-    float *cvs = reinterpret_cast<float *>(smem + L.cv);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar);
+    uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int pr = lane >> 3, j = lane & 7;
-    const int c_lo = blockIdx.y * p.cps;
-    const int c_hi = c_lo + p.cps < p.ks ? c_lo + p.cps : p.ks;
-    const int ncta = c_hi - c_lo;
-    const int g_lo = c_lo * kCG;
-    const int g_hi = c_hi * kCG < p.G ? c_hi * kCG : p.G;
-    const int gsn = g_hi - g_lo;  // groups of x staged by this CTA
-    // Row blocks of this CTA: a balanced share of all NB row blocks (persistent
-    // grid), or RB consecutive ones (one row tile per CTA).
-    int rb_lo, rb_hi;
-    if (p.balanced) {
-        rb_lo = int((long long)blockIdx.x * p.NB / gridDim.x);
-        rb_hi = int((long long)(blockIdx.x + 1) * p.NB / gridDim.x);
-    } else {
-        rb_lo = blockIdx.x * p.RB;
-        rb_hi = rb_lo + p.RB < p.NB ? rb_lo + p.RB : p.NB;
-    }
-    const int row_t0 = rb_lo * RW;
-    const int nunits = (rb_hi - rb_lo) * p.H;  // (row block, chunk phase) pairs
-    const int stage_shift = __ffs(p.stages) - 1;
+    const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+    const int C = p.consumers;
 
-    // A unit is one row block and the contiguous chunk block [cb0, cb1) of its
-    // chunk phase: groups [gw0, gw1), stage s holding groups gw0 + 8s .. + 7; a
-    // chunk ends every kSPC stages and only the unit's last stage can be partial.
+    const int c_lo = blockIdx.y * p.cpc;
+    const int c_hi = c_lo + p.cpc < p.ks ? c_lo + p.cpc : p.ks;
+    const int sub_lo = c_lo * kChunkSubs;
+    const int sub_hi = c_hi * kChunkSubs < p.S_row ? c_hi * kChunkSubs : p.S_row;
+    const int nsub = sub_hi - sub_lo;
+    const int rb_lo = int((long long)blockIdx.x * p.NB / p.grid_rows);
+    const int rb_hi = int((long long)(blockIdx.x + 1) * p.NB / p.grid_rows);
+    const int row_t0 = rb_lo * kRows;
+    const int upr = (c_hi - c_lo + p.uc - 1) / p.uc;  // units per row block
+    const int nunits = (rb_hi - rb_lo) * upr;
+    const int cpc_here = c_hi - c_lo;
+
+    const int nsub_max = p.cpc * kChunkSubs < p.S_row ? p.cpc * kChunkSubs : p.S_row;
+    const SmemLayout L = smem_layout(BITS, V, p.pitch, p.sb_mode_unit, p.sbox, p.slots, nsub_max, p.max_rb, p.cpc);
+    const uint32_t ring = smem_u32(smem + L.ring);
+    const uint32_t xs = smem_u32(smem + L.xs);
+    float *cvs = reinterpret_cast<float *>(smem + L.cv);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar);  // full[slots], empty[slots]
+    unsigned *s_next = reinterpret_cast<unsigned *>(smem + L.misc);
+    volatile unsigned *s_abort = s_next + 1;
+    // s_issued[k]: units issued by producer k (it issues k, k + P, ...).
+    volatile int *s_issued = reinterpret_cast<volatile int *>(s_next + 2);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + p.slots);
+
+    // Geometry of unit u: rows [r0, r0 + 4), chunks [c0, c1).
     struct Unit {
-        int row0, cb0, gw0, gw1, total;
+        int r0, nr, c0, c1;
     };
     auto unit_geo = [&](int u) {
-        Unit q;
-        const int rbl = u / p.H, hh = u - rbl * p.H;
-        q.row0 = (rb_lo + rbl) * RW;
-        q.cb0 = c_lo + hh * ncta / p.H;
-        const int cb1 = c_lo + (hh + 1) * ncta / p.H;
-        q.gw0 = q.cb0 * kCG;
-        q.gw1 = cb1 * kCG < p.G ? cb1 * kCG : p.G;
-        q.total = (q.gw1 - q.gw0 + kSlices - 1) / kSlices;
-        return q;
+        Unit g;
+        const int rbl = u / upr, pc = u - rbl * upr;
+        g.r0 = (rb_lo + rbl) * kRows;
+        g.nr = p.N - g.r0 < kRows ? p.N - g.r0 : kRows;
+        g.c0 = c_lo + pc * p.uc;
+        g.c1 = g.c0 + p.uc < c_hi ? g.c0 + p.uc : c_hi;
+        return g;
+    };
+    // Element coordinate of scale/bias box `bx` of a unit (rows r0.., groups from chunk c0).
+    auto sb_coord = [&](const Unit &g, int bx) {
+        const long long g0 = (long long)g.c0 * kChunkElems / GS;
+        return round_down8((long long)(g.r0 + bx) * p.G + g0);
     };
 
-    const uint32_t bar0 = smem_u32(bars + warp * p.stages);
-    const uint32_t ring_w = smem_u32(smem + L.ring + warp * p.stages * kStageBytes);
     const uint64_t pol = l2_evict_first_policy();
-
-    // Producer (lane 0): the warp's stage sequence runs through its units
-    // u = warp, warp + nwarps, ... in order; `issued` counts stages issued.
-    int pu = warp, ps = 0, issued = 0;
-    Unit pg = unit_geo(pu < nunits ? pu : 0);
-    auto issue_next = [&]() {
-        if (pu >= nunits) return;
-        const int slot = issued & (p.stages - 1);
-        const int gst = pg.gw0 + ps * kSlices;  // first group of the stage
-        int nb = (pg.gw1 - gst + kGPB - 1) / kGPB;
-        nb = nb < kBPS ? nb : kBPS;
-        mbar_arrive_expect_tx(bar0 + 8 * slot, nb * kBoxSmem);
-        for (int b = 0; b < nb; ++b)
-            tma_load_2d(ring_w + slot * kStageBytes + b * kBoxSmem, tmap_w, gst * kGB + b * kBoxBytes, pg.row0,
-                        bar0 + 8 * slot, pol);
-        ++issued;
-        if (++ps == pg.total) {
-            ps = 0;
-            pu += nwarps;
-            if (pu < nunits) pg = unit_geo(pu);
+    auto issue = [&](const Unit &g, int slot) {
+        const uint32_t base = ring + slot * L.slot_bytes;
+        const uint32_t full = full0 + 8 * slot;
+        const int e0 = g.c0 * kChunkElems;
+        const int e1 = g.c1 * kChunkElems < p.K ? g.c1 * kChunkElems : p.K;
+        const uint32_t seg = uint32_t(e1 - e0) * BITS / 8;
+        const int nbox = p.sb_mode_unit ? 1 : g.nr;
+        const uint32_t wbytes = p.full_rows ? uint32_t(g.nr) * uint32_t(p.row_bytes) : uint32_t(g.nr) * seg;
+        mbar_arrive_expect_tx(full, wbytes + uint32_t(2 * nbox * p.sbox * 2));
+        if (p.full_rows) {
+            bulk_load(base, p.w + size_t(g.r0) * p.row_bytes, wbytes, full, pol);
+        } else {
+            for (int r = 0; r < g.nr; ++r)
+                bulk_load(base + r * p.pitch, p.w + size_t(g.r0 + r) * p.row_bytes + size_t(e0) * BITS / 8, seg, full,
+                          pol);
+        }
+        for (int bx = 0; bx < nbox; ++bx) {
+            const int xc = sb_coord(g, bx);
+            tma_load_1d(base + L.sb_off + bx * L.sbs, map_s, xc, full);
+            tma_load_1d(base + L.sb_off + (nbox + bx) * L.sbs, map_b, xc, full);
         }
     };
 
-    // Weight tiles first: they do not depend on x, so their latency overlaps the staging below.
-    if (lane == 0) {
-        for (int s = 0; s < p.stages; ++s) mbar_init(bar0 + 8 * s, 1);
+    // The ring protocol needs at most one consumer warp per slot and every
+    // slot served by one producer (slots a multiple of the producer count).
+    const int P = nwarps - C;
+    if (C > p.slots || C < 1 || P < 1 || p.slots % P != 0) {
+        if (tid == 0) atomicOr(p.err, 2u);
+        return;
+    }
+    if (tid < 2 * p.slots) {  // full[] and empty[] are contiguous
+        mbar_init(full0 + 8 * tid, 1);
         fence_mbar_init();
-        for (int s = 0; s < p.stages; ++s) issue_next();
     }
-    __syncwarp();
-
-    // Stage x for groups [g_lo, g_hi): fp32, position-scaled, 8 elements per task.
-    {
-        constexpr int kUPG = GS / 8;
-        const int per_vec = gsn * kUPG, all = V * per_vec;
-        for (int u0 = tid; u0 < all; u0 += 4 * nthreads) {
-            uint4 raw[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int u = u0 + k * nthreads;
-                if (u < all) {
-                    const int v = u / per_vec, rem = u - v * per_vec;
-                    raw[k] = __ldg(reinterpret_cast<const uint4 *>(p.x + size_t(v) * p.K + size_t(g_lo) * GS) + rem);
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int u = u0 + k * nthreads;
-                if (u < all) {
-                    const int v = u / per_vec, rem = u - v * per_vec;
-                    const int gl = rem / kUPG, e8 = rem - gl * kUPG;
-                    const uint32_t w4[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
-                    float f[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const uint32_t bits = (i & 1) ? (w4[i / 2] & 0xFFFF0000u) : (w4[i / 2] << 16);
-                        const float scale = __uint_as_float(uint32_t(127 - BITS * (i % kPerHalf)) << 23);
-                        f[i] = __fmul_rn(__uint_as_float(bits), scale);
-                    }
-                    float4 *dst = reinterpret_cast<float4 *>(xs + (v * p.gsm + gl) * kXS + e8 * 8);
-                    dst[0] = make_float4(f[0], f[1], f[2], f[3]);
-                    dst[1] = make_float4(f[4], f[5], f[6], f[7]);
-                }
-            }
-        }
-        // sum(x) per (vector, group): eight sums of eight consecutive elements,
-        // each left to right, then those (eight, or sixteen for gs = 128) left to right.
-        for (int idx = tid; idx < V * gsn; idx += nthreads) {
-            const int v = idx / gsn, gl = idx - v * gsn;
-            const uint4 *src = reinterpret_cast<const uint4 *>(p.x + size_t(v) * p.K + size_t(g_lo + gl) * GS);
-            uint4 raw[kUPG];
-#pragma unroll
-            for (int k = 0; k < kUPG; ++k) raw[k] = __ldg(src + k);
-            float total_sum = 0.0f;
-#pragma unroll
-            for (int k = 0; k < kUPG; ++k) {
-                const uint32_t w4[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
-                float s8 = __uint_as_float(w4[0] << 16);
-#pragma unroll
-                for (int i = 1; i < 8; ++i)
-                    s8 = __fadd_rn(s8, __uint_as_float((i & 1) ? (w4[i / 2] & 0xFFFF0000u) : (w4[i / 2] << 16)));
-                total_sum = k == 0 ? s8 : __fadd_rn(total_sum, s8);
-            }
-            sxs[v * p.gsm + gl] = total_sum;
-        }
+    if (tid == 0) {
+        *s_next = 0;
+        *s_abort = 0;
     }
+    if (tid < P) s_issued[tid] = 0;
     __syncthreads();
+    grid_launch_dependents();
 
-    bool ok = true;
-    int consumed = 0;
-    // The magic constant and the pair (-2^23, -2^23) as register operands of the extraction.
-    uint32_t magic;
-    asm volatile("mov.b32 %0, %1;" : "=r"(magic) : "n"(kMagic));
-    const uint64_t nm = 0xCB000000CB000000ull;
-    // Per-lane byte offsets, inside a stage, of the first chunk of slice j's
-    // group for each of the lane's rows (128B swizzle: chunk index XOR row % 8).
-    uint32_t woff[R];
-    {
-        constexpr int kChunks = kGB / 16;
-        const int c0 = (j % kGPB) * kChunks;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int row = pr + 4 * r;
-            woff[r] = uint32_t((j / kGPB) * kBoxSmem + row * kBoxBytes + ((c0 ^ (row & 7)) << 4));
+    if (warp >= C) {
+        // --------------------------------------------------------- producers
+        // Producer k issues units k, k + P, ... (so it alone serves the slots
+        // congruent to k modulo P), each after the slot's previous unit was
+        // consumed. Weight, scale and bias tiles do not depend on the
+        // preceding grid, so the producers never wait for it (nor for x).
+        const int kp = warp - C;
+        bool ok = true;
+        int slot = kp, lap = 0, rbl = 0, pc = kp;
+        while (pc >= upr) {
+            pc -= upr;
+            ++rbl;
         }
-    }
-    const uint32_t ring_s = smem_u32(smem + L.ring);
-    const uint32_t xs_s = smem_u32(xs);
-
-    for (int u = warp; u < nunits && ok; u += nwarps) {
-        const Unit q = unit_geo(u);
-        const int rbl = u / p.H;
-        // Scale and bias of the lane's group, loaded one stage ahead.
-        const uint16_t *srow[R], *brow[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int n = q.row0 + pr + 4 * r < p.N ? q.row0 + pr + 4 * r : p.N - 1;
-            srow[r] = p.scales + size_t(n) * p.G;
-            brow[r] = p.biases + size_t(n) * p.G;
-        }
-        uint16_t ms[R], mb[R];
-        {
-            const int g = q.gw0 + j < q.gw1 ? q.gw0 + j : q.gw1 - 1;
-#pragma unroll
-            for (int r = 0; r < R; ++r) { ms[r] = __ldg(srow[r] + g); mb[r] = __ldg(brow[r] + g); }
-        }
-        float part[R][V];
-        for (int s = 0; s < q.total; ++s) {
-            const int t = s & (kSPC - 1);
-            if (t == 0) {
-#pragma unroll
-                for (int r = 0; r < R; ++r)
-#pragma unroll
-                    for (int v = 0; v < V; ++v) part[r][v] = 0.0f;
+        for (int u = kp; u < nunits; u += P) {
+            if (lane == 0) {
+                if (lap > 0) ok = !*s_abort && mbar_wait_bounded(empty0 + 8 * slot, (lap - 1) & 1);
+                if (ok) {
+                    Unit g;
+                    g.r0 = (rb_lo + rbl) * kRows;
+                    g.nr = p.N - g.r0 < kRows ? p.N - g.r0 : kRows;
+                    g.c0 = c_lo + pc * p.uc;
+                    g.c1 = g.c0 + p.uc < c_hi ? g.c0 + p.uc : c_hi;
+                    issue(g, slot);
+                    __threadfence_block();
+                    s_issued[kp] = u + 1;
+                }
             }
-            float fs[R], fb[R];
-#pragma unroll
-            for (int r = 0; r < R; ++r) { fs[r] = bf16_bits_to_f32(ms[r]); fb[r] = bf16_bits_to_f32(mb[r]); }
-            const int g = q.gw0 + s * kSlices + j;
-            if (s + 1 < q.total) {
-                const int gn = g + kSlices < q.gw1 ? g + kSlices : q.gw1 - 1;
-#pragma unroll
-                for (int r = 0; r < R; ++r) { ms[r] = __ldg(srow[r] + gn); mb[r] = __ldg(brow[r] + gn); }
-            }
-            const int slot = consumed & (p.stages - 1);
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar0 + 8 * slot, (consumed >> stage_shift) & 1));
+            ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
-            if (g < q.gw1) {
-                const int gl = g - g_lo;
-                uint64_t acc[R][V];
-                group_dot<BITS, GS, V, R>(ring_s + (warp * p.stages + slot) * kStageBytes, woff,
-                                          xs_s + gl * kXS * 4, p.gsm * kXS * 4, magic, nm, acc);
+            slot += P;
+            if (slot >= p.slots) {
+                slot -= p.slots;
+                ++lap;
+            }
+            pc += P;
+            while (pc >= upr) {
+                pc -= upr;
+                ++rbl;
+            }
+        }
+        if (!ok && lane == 0) {
+            atomicOr(p.err, 1u);
+            *s_abort = 1;
+        }
+    } else {
+        // x may be written by the preceding grid: wait for it.
+        grid_dependency_wait();
+        // Stage x of subgroups [sub_lo, sub_hi) for every vector: eight threads
+        // per subgroup, eight elements each (steps 1 and 2 of the fixed order).
+        {
+            const int per_vec = nsub * 8, all = V * per_vec;
+            const int nct = C * 32;  // consumer threads
+            const int all_pad = (all + nct - 1) / nct * nct;
+            for (int u = tid; u < all_pad; u += nct) {
+                const bool live = u < all;
+                const int v = live ? u / per_vec : 0;
+                const int rem = live ? u - v * per_vec : 0;
+                const int sl = rem >> 3, e8 = rem & 7;  // subgroup (CTA-local), eighth
+                uint4 raw = make_uint4(0, 0, 0, 0);
+                if (live)
+                    raw = __ldg(reinterpret_cast<const uint4 *>(p.x + size_t(v) * p.K + size_t(sub_lo + sl) * kSub) + e8);
+                const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+                uint32_t e = 1;
+                float xv[8];
+    #pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t bits = (i & 1) ? (w4[i / 2] >> 16) : (w4[i / 2] & 0xFFFFu);
+                    xv[i] = bf16_bits_to_f32(bits);
+                    const uint32_t f = (bits >> 7) & 0xFFu;
+                    e = f > e ? f : e;
+                }
+                // largest exponent field of the subgroup (its eight threads are eight consecutive lanes)
+    #pragma unroll
+                for (int m = 1; m < 8; m <<= 1) {
+                    const uint32_t o = __shfl_xor_sync(0xffffffffu, e, m);
+                    e = o > e ? o : e;
+                }
+                // x' = x * 2^(254 - bits*k - E), as two exact power-of-two factors
+                float xr[8];
+    #pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int k = BITS == 4 ? (i & 3) : i;
+                    const int pw = 254 - BITS * k - int(e);
+                    const int p1 = pw < 127 ? pw : 127;
+                    const float m1 = __uint_as_float(uint32_t(p1 + 127) << 23);
+                    const float m2 = __uint_as_float(uint32_t(pw - p1 + 127) << 23);
+                    xr[i] = bf16_round(__fmul_rn(__fmul_rn(xv[i], m1), m2));
+                }
+                // eight-element sum, left to right; the subgroup's sum gathers the eight in order
+                float s8 = xv[0];
+    #pragma unroll
+                for (int i = 1; i < 8; ++i) s8 = __fadd_rn(s8, xv[i]);
+                float sx = 0.0f;
+    #pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float o = __shfl_sync(0xffffffffu, s8, i, 8);
+                    sx = i == 0 ? o : __fadd_rn(sx, o);
+                }
+                if (live) {
+                    const int t = sub_lo + sl;  // subgroup index in the row
+                    // octet position of these eight elements in processing order
+                    const int oct = BITS == 4 ? (e8 ^ (((t >> 2) & 1) * 4)) : e8;
+                    if constexpr (V == 1) {
+                        float4 *dst = reinterpret_cast<float4 *>(smem + L.xs + size_t(sl) * kXsF32 * 4 + oct * 32);
+                        dst[0] = make_float4(xr[0], xr[1], xr[2], xr[3]);
+                        dst[1] = make_float4(xr[4], xr[5], xr[6], xr[7]);
+                    } else {
+                        uint32_t pk[4];
+    #pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            pk[i] = (__float_as_uint(xr[2 * i]) >> 16) | (__float_as_uint(xr[2 * i + 1]) & 0xFFFF0000u);
+                        *reinterpret_cast<uint4 *>(smem + L.xs + (size_t(v) * nsub_max + sl) * kXsB16 + oct * 16) =
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                    if (e8 == 0) {
+                        const int c = int(e) - 105;  // f1 * f2 = 2^c
+                        const int c1 = c < 127 ? c : 127;
+                        const float4 meta = make_float4(sx, __uint_as_float(uint32_t(c1 + 127) << 23),
+                                                        __uint_as_float(uint32_t(c - c1 + 127) << 23), 0.0f);
+                        if constexpr (V == 1)
+                            *reinterpret_cast<float4 *>(smem + L.xs + size_t(sl) * kXsF32 * 4 + 256) = meta;
+                        else
+                            *reinterpret_cast<float4 *>(smem + L.xs + (size_t(v) * nsub_max + sl) * kXsB16 + 128) = meta;
+                    }
+                }
+            }
+        }
+        // consumer warps only
+        asm volatile("bar.sync 1, %0;" ::"r"(C * 32) : "memory");
+
+        // --------------------------------------------------------- consumers
+        uint32_t poff[T::NP];
+        piece_offsets<BITS>(lane, poff);
+        const uint32_t xv_bytes = uint32_t(nsub_max) * kXsB16;
+        for (;;) {
+            int u = 0;
+            if (lane == 0) u = int(atomicAdd(s_next, 1u));
+            u = __shfl_sync(0xffffffffu, u, 0);
+            if (u >= nunits) break;
+            const int slot = u % p.slots;
+            // Wait by phase parity only once unit u is issued: issuing it
+            // required the slot's previous unit to be consumed, so the slot's
+            // barrier is then in the phase of unit u or just past it (data
+            // may arrive out of order, so grabbing alone does not ensure that).
+            bool ok = !*s_abort;
+            if (ok) ok = wait_issued(s_issued + u % P, u);
+            if (ok) ok = mbar_wait_bounded(full0 + 8 * slot, (u / p.slots) & 1);
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) {
+                    atomicOr(p.err, 1u);
+                    *s_abort = 1;
+                }
+                break;
+            }
+            const Unit g = unit_geo(u);
+            const uint32_t base = ring + slot * L.slot_bytes;
+            const int nbox = p.sb_mode_unit ? 1 : g.nr;
+            for (int cc = g.c0; cc < g.c1; ++cc) {
+                const int t = cc * kChunkSubs + lane;        // subgroup index in the row
+                const bool active = t < p.S_row;
+                const int tl = active ? t : cc * kChunkSubs;  // a valid subgroup for idle lanes
+                const int ln = tl - cc * kChunkSubs;
+                // chunk offset inside a slot row
+                const uint32_t coff = uint32_t(p.full_rows ? cc * kChunkB : (cc - g.c0) * kChunkB);
+                uint32_t wrow[kRows][T::NP];
 #pragma unroll
-                for (int v = 0; v < V; ++v) {
-                    const float sx = sxs[v * p.gsm + gl];
+                for (int r = 0; r < kRows; ++r)
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const float d = __fadd_rn(pair_lo(acc[r][v]), pair_hi(acc[r][v]));
-#if defined(QMV_TEST_MUTATE_ORDER)
-                        // Test-only build: the streamed kernel folds bias before scale,
-                        // so the bit-identity tests can show they detect an order change.
-                        if constexpr (V > 1) {
-                            part[r][v] = __fmaf_rn(fb[r], sx, part[r][v]);
-                            part[r][v] = __fmaf_rn(fs[r], d, part[r][v]);
-                            continue;
+                    for (int pc = 0; pc < T::NP; ++pc)
+                        wrow[r][pc] = base + r * p.pitch + coff + (active ? poff[pc] : poff[pc] - lane * kSubB + ln * kSubB);
+                // scale and bias of the lane's group in each row
+                const int gi = int((long long)tl * kSub / GS);
+                float fs[kRows], fb[kRows];
+#pragma unroll
+                for (int r = 0; r < kRows; ++r) {
+                    const int bx = p.sb_mode_unit ? 0 : (r < g.nr ? r : 0);
+                    const int off = int((long long)(g.r0 + r) * p.G + gi - sb_coord(g, bx));
+                    const int offc = r < g.nr ? off : 0;
+                    fs[r] = bf16_bits_to_f32(lds_u16(base + L.sb_off + bx * L.sbs + offc * 2));
+                    fb[r] = bf16_bits_to_f32(lds_u16(base + L.sb_off + (nbox + bx) * L.sbs + offc * 2));
+                }
+                const int sl = tl - sub_lo;
+                if constexpr (V == 1) {
+                    const uint32_t xsub = xs + uint32_t(sl) * kXsF32 * 4;
+                    uint64_t acc[kRows];
+                    subgroup_dot_v1<BITS>(wrow, xsub, acc);
+                    const float4 meta = lds_f4(xsub + 256);
+                    float val[T::NRED];
+#pragma unroll
+                    for (int r = 0; r < kRows; ++r) {
+                        const float term = subgroup_term<false>(acc[r], fs[r], fb[r], meta.x, meta.y, meta.z);
+                        val[r] = active ? term : 0.0f;
+                    }
+                    const float tot = tree_reduce_scatter<T::NRED>(val, lane);
+                    const int r = lane >> 3;
+                    if ((lane & 7) == 0 && r < g.nr)
+                        cvs[(g.r0 - row_t0 + r) * cpc_here + (cc - c_lo)] = tot;
+                } else {
+#pragma unroll
+                    for (int ps = 0; ps < T::PASSES; ++ps) {
+                        const int v0 = ps * T::VP;
+                        const uint32_t xsub = xs + (uint32_t(v0) * nsub_max + sl) * kXsB16;
+                        uint64_t acc[kRows][T::VP];
+                        subgroup_dot_vp<BITS, T::VP>(wrow, xsub, xv_bytes, acc);
+                        float val[T::NRED];
+#pragma unroll
+                        for (int i = 0; i < T::NRED; ++i) val[i] = 0.0f;
+#pragma unroll
+                        for (int v = 0; v < T::VP; ++v) {
+                            if (v0 + v >= V) break;
+                            const float4 meta = lds_f4(xsub + v * xv_bytes + 128);
+#pragma unroll
+                            for (int r = 0; r < kRows; ++r) {
+                                const float term = subgroup_term<true>(acc[r][v], fs[r], fb[r], meta.x, meta.y, meta.z);
+                                val[r * T::VP + v] = active ? term : 0.0f;
+                            }
                         }
-#endif
-                        part[r][v] = __fmaf_rn(fs[r], d, part[r][v]);
-                        part[r][v] = __fmaf_rn(fb[r], sx, part[r][v]);
+                        const float tot = tree_reduce_scatter<T::NRED>(val, lane);
+                        // lane holds value index lane >> (5 - log2 NRED)
+                        constexpr int SH = T::NRED == 4 ? 3 : T::NRED == 8 ? 2 : T::NRED == 16 ? 1 : 0;
+                        const int idx = lane >> SH;
+                        const int r = idx / T::VP, v = idx - r * T::VP;
+                        if ((lane & ((1 << SH) - 1)) == 0 && idx < T::NVAL && v0 + v < V && r < g.nr)
+                            cvs[((g.r0 - row_t0 + r) * cpc_here + (cc - c_lo)) * V + v0 + v] = tot;
                     }
                 }
             }
             __syncwarp();
-            ++consumed;
-            if (lane == 0) {
-                fence_proxy_async_smem();
-                issue_next();
-            }
-            // End of a chunk: butterfly over the slices, chunk value to shared memory.
-            if (t == kSPC - 1 || s == q.total - 1) {
-                float *cv = cvs + ((q.cb0 + s / kSPC - c_lo) * tile_rows + rbl * RW) * V;
-#pragma unroll
-                for (int v = 0; v < V; ++v)
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        float x1 = part[r][v];
-                        x1 = __fadd_rn(x1, __shfl_xor_sync(0xffffffffu, x1, 4));
-                        x1 = __fadd_rn(x1, __shfl_xor_sync(0xffffffffu, x1, 2));
-                        x1 = __fadd_rn(x1, __shfl_xor_sync(0xffffffffu, x1, 1));
-                        if ((v & 7) == j) cv[(pr + 4 * r) * V + v] = x1;
-                    }
-            }
+            if (lane == 0) mbar_arrive(empty0 + 8 * slot);
         }
     }
-    if (!ok && lane == 0) {
-        // Record the failure, then wait (bounded) for this warp's own copies
-        // still in flight before the CTA may exit.
-        atomicOr(p.err, 1u);
-        for (int s2 = consumed; s2 < issued; ++s2)
-            (void)mbar_wait_bounded(bar0 + 8 * (s2 & (p.stages - 1)), (s2 >> stage_shift) & 1);
-    }
     __syncthreads();
+    if (*s_abort) {
+        // Wait (bounded) for every copy this CTA may still have in flight.
+        if (warp >= C && lane == 0) {
+            const int kp = warp - C;
+            const int hi = s_issued[kp];
+            for (int u = hi - p.slots > kp ? hi - p.slots : kp; u < hi; u += P)
+                (void)mbar_wait_bounded(full0 + 8 * (u % p.slots), (u / p.slots) & 1);
+        }
+        __syncthreads();
+        return;
+    }
 
     auto store_y = [&](int v, int n, float val) {
         if (p.f32_out)
@@ -541,37 +760,39 @@ __device__ __forceinline__ void qmv_body(const CUtensorMap *tmap_w, const Params
         else
             static_cast<__nv_bfloat16 *>(p.y)[size_t(v) * p.N + n] = __float2bfloat16_rn(val);
     };
-    const int nrows = (rb_hi - rb_lo) * RW;
+    const int nrows = (rb_hi - rb_lo) * kRows;
 
     // Step 4: fold the chunk values left to right.
-    if (p.cps == p.ks) {
+    if (p.cpc >= p.ks) {
         for (int idx = tid; idx < nrows * V; idx += nthreads) {
-            const int r = idx / V, v = idx - r * V;
+            const int v = idx / nrows, r = idx - v * nrows;
             const int n = row_t0 + r;
             if (n >= p.N) continue;
-            float acc = cvs[r * V + v];
-            for (int c = 1; c < p.ks; ++c) acc = __fadd_rn(acc, cvs[(c * tile_rows + r) * V + v]);
+            float acc = cvs[(r * cpc_here) * V + v];
+            for (int c = 1; c < p.ks; ++c) acc = __fadd_rn(acc, cvs[(r * cpc_here + c) * V + v]);
             store_y(v, n, acc);
         }
         return;
     }
 
-    // One chunk per CTA: publish its values; the CTA that completes the row
-    // tile last folds all chunks left to right and zeroes what it read, so
-    // (with the self-resetting counter) the workspace is zero again.
-    for (int idx = tid; idx < nrows * V; idx += nthreads) {
-        const int r = idx / V, v = idx - r * V;
+    // A chunk range per CTA: publish its values; the CTA that completes the
+    // row range last folds all chunks left to right and zeroes what it read,
+    // so (with the self-resetting counter) the workspace is zero again.
+    for (int idx = tid; idx < nrows * V * cpc_here; idx += nthreads) {
+        const int cl = idx / (nrows * V), rem = idx - cl * nrows * V;
+        const int v = rem / nrows, r = rem - v * nrows;
         const int n = row_t0 + r;
-        if (n < p.N) __stcg(p.partials + (size_t(c_lo) * V + v) * p.N + n, cvs[r * V + v]);
+        if (n < p.N) __stcg(p.partials + (size_t(c_lo + cl) * V + v) * p.N + n, cvs[(r * cpc_here + cl) * V + v]);
     }
     __threadfence();
     __syncthreads();
-    if (tid == 0) s_ticket = atomicInc(p.counters + blockIdx.x, unsigned(p.ks - 1));
+    const unsigned nranges = unsigned(gridDim.y);
+    if (tid == 0) s_ticket = atomicInc(p.counters + rb_lo, nranges - 1);
     __syncthreads();
-    if (s_ticket != unsigned(p.ks - 1)) return;
+    if (s_ticket != nranges - 1) return;
     __threadfence();
     for (int idx = tid; idx < nrows * V; idx += nthreads) {
-        const int r = idx % nrows, v = idx / nrows;
+        const int v = idx / nrows, r = idx - v * nrows;
         const int n = row_t0 + r;
         if (n >= p.N) continue;
         float *pp = p.partials + size_t(v) * p.N + n;
@@ -586,19 +807,23 @@ __device__ __forceinline__ void qmv_body(const CUtensorMap *tmap_w, const Params
     }
 }
 
-// Rows per lane R: the single-vector kernel comes with R = 2 and R = 4 (the
-// host picks by shape); the streamed kernel uses R = 2 (its registers go to V).
-template <int BITS, int GS, int R>
-__global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_m1(const __grid_constant__ CUtensorMap tmap_w, const Params p)
+// Launch bounds: V = 1 runs 16 consumer warps + 4 producers; the streamed
+// kernel 10 + 2 (its registers go to the V-vector accumulators).
+constexpr int kThreadsV1 = 20 * 32;
+constexpr int kThreadsVN = 12 * 32;
+
+template <int BITS, int GS>
+__global__ void __launch_bounds__(kThreadsV1, 1)
+    qmv_m1(const __grid_constant__ CUtensorMap map_s, const __grid_constant__ CUtensorMap map_b, const Params p)
 {
-    qmv_body<BITS, GS, 1, R>(&tmap_w, p);
+    qmv_body<BITS, GS, 1>(&map_s, &map_b, p);
 }
 
 template <int BITS, int GS, int V>
-__global__ void __launch_bounds__(kMaxWarps * 16, (V <= 4 ? 2 : 1))
-    qmv_streamed(const __grid_constant__ CUtensorMap tmap_w, const Params p)
+__global__ void __launch_bounds__(kThreadsVN, 1)
+    qmv_streamed(const __grid_constant__ CUtensorMap map_s, const __grid_constant__ CUtensorMap map_b, const Params p)
 {
-    qmv_body<BITS, GS, V, 2>(&tmap_w, p);
+    qmv_body<BITS, GS, V>(&map_s, &map_b, p);
 }
 
 }  // namespace qmv

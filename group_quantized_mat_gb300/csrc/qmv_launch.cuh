@@ -9,8 +9,8 @@
 namespace qmv {
 
 template <typename Kern>
-cudaError_t launch_one(Kern kern, int (&configured)[64], const CUtensorMap &map, const Params &p, dim3 grid,
-                       int threads, size_t smem, cudaStream_t stream)
+cudaError_t launch_one(Kern kern, int (&configured)[64], const CUtensorMap &map_s, const CUtensorMap &map_b,
+                       const Params &p, const Launch &l, cudaStream_t stream)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -18,36 +18,44 @@ cudaError_t launch_one(Kern kern, int (&configured)[64], const CUtensorMap &map,
     if (dev >= 64) return cudaErrorInvalidDevice;
     // The opt-in dynamic shared-memory limit is a per-device kernel attribute;
     // raise it when this launch needs more than it was last set to.
-    if (configured[dev] < int(smem)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (configured[dev] < int(l.smem)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(l.smem));
         if (e != cudaSuccess) return e;
-        configured[dev] = int(smem);
+        configured[dev] = int(l.smem);
     }
-    kern<<<grid, threads, smem, stream>>>(map, p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = l.grid;
+    cfg.blockDim = dim3(l.threads);
+    cfg.dynamicSmemBytes = l.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = l.pdl ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, kern, map_s, map_b, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 template <int BITS, int GS, int V>
-cudaError_t launch_v(int R, const CUtensorMap &map, const Params &p, dim3 grid, int threads, size_t smem,
+cudaError_t launch_v(const CUtensorMap &map_s, const CUtensorMap &map_b, const Params &p, const Launch &l,
                      cudaStream_t stream)
 {
-    if constexpr (V == 1) {
-        static int configured2[64] = {0}, configured4[64] = {0};
-        if (R == 4) return launch_one(qmv_m1<BITS, GS, 4>, configured4, map, p, grid, threads, smem, stream);
-        return launch_one(qmv_m1<BITS, GS, 2>, configured2, map, p, grid, threads, smem, stream);
-    } else {
-        static int configured[64] = {0};
-        return launch_one(qmv_streamed<BITS, GS, V>, configured, map, p, grid, threads, smem, stream);
-    }
+    static int configured[64] = {0};
+    if constexpr (V == 1)
+        return launch_one(qmv_m1<BITS, GS>, configured, map_s, map_b, p, l, stream);
+    else
+        return launch_one(qmv_streamed<BITS, GS, V>, configured, map_s, map_b, p, l, stream);
 }
 
 template <int BITS, int GS>
-cudaError_t launch_bits_gs(int V, int R, const CUtensorMap &map, const Params &p, dim3 grid, int threads,
-                           size_t smem, cudaStream_t stream)
+cudaError_t launch_bits_gs(int V, const CUtensorMap &map_s, const CUtensorMap &map_b, const Params &p,
+                           const Launch &l, cudaStream_t stream)
 {
     switch (V) {
 #define QMV_CASE(v) \
-    case v: return launch_v<BITS, GS, v>(R, map, p, grid, threads, smem, stream);
+    case v: return launch_v<BITS, GS, v>(map_s, map_b, p, l, stream);
         QMV_CASE(1) QMV_CASE(2) QMV_CASE(3) QMV_CASE(4) QMV_CASE(5) QMV_CASE(6) QMV_CASE(7) QMV_CASE(8)
         QMV_CASE(9) QMV_CASE(10) QMV_CASE(11) QMV_CASE(12) QMV_CASE(13) QMV_CASE(14) QMV_CASE(15) QMV_CASE(16)
 #undef QMV_CASE

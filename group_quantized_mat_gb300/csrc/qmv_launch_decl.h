@@ -8,12 +8,21 @@
 
 namespace qmv {
 
-// Warps a CTA may have for this V (the kernels' launch bounds).
-inline int max_warps(int V) { return V == 1 ? 16 : 8; }
+// Warps per CTA of the kernel for V vectors (its launch bounds): consumer
+// warps, then producer warps.
+inline int consumer_warps(int V) { return V == 1 ? 16 : 10; }
+inline int producer_warps(int V) { return V == 1 ? 4 : 2; }
 
-#define QMV_DECLARE_LAUNCH(name)                                                                            \
-    cudaError_t name(int V, int R, const CUtensorMap &map, const Params &p, dim3 grid, int threads, \
-                     size_t smem, cudaStream_t stream);
+struct Launch {
+    dim3 grid;
+    int threads;
+    size_t smem;
+    bool pdl;  // launch with a programmatic dependency on the preceding grid
+};
+
+#define QMV_DECLARE_LAUNCH(name) \
+    cudaError_t name(int V, const CUtensorMap &map_s, const CUtensorMap &map_b, const Params &p, const Launch &l, \
+                     cudaStream_t stream);
 QMV_DECLARE_LAUNCH(launch_b4g64)
 QMV_DECLARE_LAUNCH(launch_b4g128)
 QMV_DECLARE_LAUNCH(launch_b2g64)

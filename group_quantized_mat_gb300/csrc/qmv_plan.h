@@ -1,88 +1,91 @@
 // Problem geometry shared by the host launcher and the kernels.
 //
-// The fp32 summation order of an output is fixed by the group size and the
-// K-chunks below, which depend on K and group_size alone. They never depend on
-// M, on the CTA shape or on the GPU: that is what keeps column j of an
-// M-vector call bit-identical to an M = 1 call on the same vector (mlxcel
-// issue #1289, "The observation this rests on").
+// The fp32 summation order of an output is fixed by K alone (64-element
+// subgroups, 2048-element chunks). It never depends on M, on the CTA shape or
+// on the GPU: that is what keeps column j of an M-vector call bit-identical to
+// an M = 1 call on the same vector (mlxcel issue #1289, "The observation this
+// rests on").
 #pragma once
 
 #include <cstdint>
 
 namespace qmv {
 
-constexpr int kSlices = 8;          // lanes sharing a row; slice j takes groups j, j+8, ... of a chunk
-constexpr int kChunkElems = 2048;   // K elements per chunk (the last chunk of a row may be shorter)
-constexpr int kBoxBytes = 128;      // TMA box inner extent = 128B swizzle span
+constexpr int kSub = 64;            // elements per subgroup: one lane's share of a chunk row
+constexpr int kChunkSubs = 32;      // subgroups per chunk, one per lane of a warp
+constexpr int kChunkElems = kSub * kChunkSubs;
+constexpr int kRows = 4;            // rows per work unit; every lane of the warp works on all of them
 constexpr int kMaxM = 16;
-constexpr int kMaxWarps = 16;       // warps per CTA
-constexpr int kMaxChunksPerCta = 64;
+constexpr int kXsF32 = 68;          // floats per staged subgroup, fp32 layout: 64 x' + (sx, f1, f2, 0)
+constexpr int kXsB16 = 144;         // bytes per staged subgroup, bf16 layout: 128 B x' + (sx, f1, f2, 0)
+constexpr int kBoxAlign = 128;      // shared-memory alignment of a tensor-map box
 
-__host__ __device__ constexpr int group_bytes(int bits, int gs) { return gs * bits / 8; }
-__host__ __device__ constexpr int groups_per_box(int bits, int gs) { return kBoxBytes / group_bytes(bits, gs); }
-__host__ __device__ constexpr int boxes_per_stage(int bits, int gs) { return kSlices * group_bytes(bits, gs) / kBoxBytes; }
-__host__ __device__ constexpr int chunk_groups(int gs) { return kChunkElems / gs; }  // a multiple of kSlices
-__host__ __device__ constexpr int x_stride(int gs) { return gs + 4; }               // floats per staged group
+__host__ __device__ constexpr int sub_bytes(int bits) { return kSub * bits / 8; }
+__host__ __device__ constexpr int chunk_bytes(int bits) { return kChunkElems * bits / 8; }
+__host__ __device__ inline int subs_per_row(int K) { return K / kSub; }
+// Number of K-chunks of a row (the last one may hold fewer than 32 subgroups).
+__host__ __device__ inline int chunk_count(int K) { return (subs_per_row(K) + kChunkSubs - 1) / kChunkSubs; }
+__host__ __device__ inline int round_down8(long long v) { return int(v & ~7ll); }
 
-// Number of K-chunks of a row: ceil(G / chunk_groups).
-__host__ __device__ inline int chunk_count(int K, int gs)
-{
-    const int G = K / gs;
-    return (G + chunk_groups(gs) - 1) / chunk_groups(gs);
-}
-
-// Kernel arguments other than the weight tensor map.
+// Kernel arguments other than the tensor maps.
 //
-// A CTA owns up to RB row blocks (4R rows each) and the chunks
-// [blockIdx.y * cps, blockIdx.y * cps + cps). Its work units are (row block,
-// chunk phase) pairs, a chunk phase being one of H contiguous blocks of the
-// CTA's chunks; warp w processes units w, w + warps, ... Chunk values meet in
-// shared memory; with cps = ks the CTA folds them into y, otherwise they go
-// through the workspace and the CTA that completes a row tile last folds all
-// ks of them.
+// CTA (i, j) owns the row blocks [i*NB/grid_rows, (i+1)*NB/grid_rows) (4 rows
+// each) and the chunks [j*cpc, min((j+1)*cpc, ks)). Its work units are
+// (row block, piece) pairs, a piece being uc consecutive chunks of the CTA's
+// range; unit u = row block u / upr, piece u % upr. One producer warp streams
+// the units in order through a ring of `slots` shared-memory slots; the
+// consumer warps take units dynamically. Chunk values meet in shared memory;
+// with cpc = ks the CTA folds them into y, otherwise they go through the
+// workspace and the CTA that completes a row range last folds all ks of them.
 struct Params {
-    const uint16_t *scales;   // bf16 bits [N, G]
-    const uint16_t *biases;   // bf16 bits [N, G]
+    const uint8_t *w;         // packed weights [N, row_bytes]
     const uint16_t *x;        // bf16 bits [V, K]
     void *y;                  // bf16 bits or float [V, N]
-    float *partials;          // [ks, V, N] when cps < ks
-    unsigned *counters;       // [ntiles] when cps < ks, zero between calls
+    float *partials;          // [ks, V, N] when cpc < ks
+    unsigned *counters;       // [NB] (one per first row block of a range) when cpc < ks; zero between calls
     unsigned *err;            // device error word
-    int N, K, G;
+    int N, K, G;              // G = K / group_size
+    int S_row;                // subgroups per row
     int ks;                   // chunks per row
-    int cps;                  // chunks per CTA: ks or 1
-    int RB, H;                // row blocks (at most) and chunk phases per CTA
-    int warps;                // warps per CTA; warp w takes units w, w + warps, ...
-    int NB;                   // row blocks of the matrix (ceil(N / rows per block))
-    int balanced;             // 1: CTA i takes row blocks [i*NB/grid, (i+1)*NB/grid)
-    int stages;               // weight stages in flight per warp (a power of two)
-    int gsm;                  // groups of x one CTA stages (its chunk range)
-    int ntiles;               // row tiles (counters) when cps < ks
+    int row_bytes;
+    int NB;                   // row blocks of the matrix
+    int grid_rows;            // CTAs along the rows
+    int cpc;                  // chunks per CTA
+    int uc;                   // chunks per unit
+    int full_rows;            // 1: a unit is whole rows, loaded as one contiguous copy
+    int pitch;                // bytes per unit row in a slot
+    int sb_mode_unit;         // 1: one scale box and one bias box per unit; 0: one of each per row
+    int sbox;                 // elements per scale / bias box (a multiple of 8)
+    int slots;                // ring slots
+    int consumers;            // consumer warps; the producer is warp `consumers`
+    int max_rb;               // row blocks of the largest CTA share
     int f32_out;
 };
 
-// Shared memory of one CTA, as byte offsets from a 1024-aligned base.
+// Shared memory of one CTA, as byte offsets from a 128-aligned base.
 struct SmemLayout {
-    int ring, xs, sx, cv, bar, total;
+    int slot_bytes, sb_off, sbs;  // slot size, offset of the scale/bias boxes in a slot, bytes per box
+    int ring, xs, cv, bar, misc, total;
 };
 
-// rows_per_block = 4 * R; one stage = boxes_per_stage boxes of (128 B x rows_per_block).
-__host__ __device__ inline int stage_bytes(int bits, int gs, int rows_per_block)
-{
-    return boxes_per_stage(bits, gs) * kBoxBytes * rows_per_block;
-}
+__host__ __device__ inline int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
-__host__ __device__ inline SmemLayout smem_layout(int bits, int gs, int V, int rows_per_block, int warps, int stages,
-                                                  int gsm, int cps, int tile_rows)
+// nsub: subgroups of x the CTA stages (per vector); V: vectors.
+__host__ __device__ inline SmemLayout smem_layout(int bits, int V, int pitch, int sb_mode_unit, int sbox, int slots,
+                                                  int nsub, int max_rb, int cpc)
 {
+    (void)bits;
     SmemLayout L;
+    L.sbs = align_up(sbox * 2, kBoxAlign);
+    L.sb_off = align_up(kRows * pitch, kBoxAlign);
+    L.slot_bytes = L.sb_off + (sb_mode_unit ? 2 : 2 * kRows) * L.sbs;
     L.ring = 0;
-    L.xs = warps * stages * stage_bytes(bits, gs, rows_per_block);
-    L.sx = L.xs + V * gsm * x_stride(gs) * 4;
-    L.cv = L.sx + V * gsm * 4;
-    L.bar = (L.cv + cps * tile_rows * V * 4 + 15) & ~15;
-    const int end = L.bar + warps * stages * 8;
-    L.total = end + 1024;  // slack for aligning the dynamic base to 1024 bytes
+    L.xs = slots * L.slot_bytes;
+    const int xs_bytes = V == 1 ? nsub * kXsF32 * 4 : V * nsub * kXsB16;
+    L.cv = align_up(L.xs + xs_bytes, 16);
+    L.bar = align_up(L.cv + max_rb * kRows * cpc * V * 4, 16);
+    L.misc = L.bar + 2 * slots * 8;
+    L.total = L.misc + 32 + kBoxAlign;  // next-unit counter, abort flag, issued counts; alignment slack
     return L;
 }
 

@@ -49,10 +49,11 @@ typedef enum qmv_status {
     QMV_ERR_NULL = 1,       /* a required pointer is NULL                                  */
     QMV_ERR_BITS = 2,       /* bits is not 2 or 4                                          */
     QMV_ERR_GROUP = 3,      /* group_size is not 64 or 128                                 */
-    QMV_ERR_SHAPE = 4,      /* N < 1, K < 1, K % group_size != 0, or a size overflows      */
+    QMV_ERR_SHAPE = 4,      /* N < 1, K < 1, K % group_size != 0, or a size overflows
+                               (N > 2^30, K > 2^24, N * K / group_size >= 2^31)          */
     QMV_ERR_M_RANGE = 5,    /* M is not in [1, QMV_MAX_M]                                  */
-    QMV_ERR_ALIGN = 6,      /* w_q, x or workspace not 16-byte aligned; scales, biases or y
-                               not 2-byte aligned (4 for an fp32 y)                       */
+    QMV_ERR_ALIGN = 6,      /* w_q, x, scales, biases or workspace not 16-byte aligned;
+                               y not 2-byte aligned (4 for an fp32 y)                     */
     QMV_ERR_CUDA = 7,       /* a CUDA runtime call failed (launch, device query, encode)   */
     QMV_ERR_WORKSPACE = 8,  /* workspace is smaller than qmv_workspace_size()              */
     QMV_ERR_VALUE = 9,      /* qmv_pack: an input value does not fit in `bits` bits        */
@@ -88,14 +89,15 @@ QMV_API qmv_status qmv_unpack(const uint32_t *w_q, uint8_t *q, int64_t N, int64_
 
 /* ------------------------------------------------------------------- plan */
 
-/* Number of contiguous K-splits the kernels use for a (N, K, bits, group_size)
- * problem, or 0 for invalid arguments. It depends on K, bits and group_size
- * only -- never on M -- so the fp32 summation order of every output is the
- * same for every M (the basis of the bit-identity guarantee below). */
+/* Number of K-chunks (2048 elements each, the last one possibly shorter) that
+ * fix the fp32 summation order of a (N, K, bits, group_size) problem, or 0 for
+ * invalid arguments. It depends on K only -- never on M -- so the order of
+ * every output is the same for every M (the basis of the bit-identity
+ * guarantee below). */
 QMV_API int qmv_split_count(int N, int K, int bits, int group_size);
 
-/* Bytes of device workspace a call with these arguments needs (0 when the
- * problem has a single K-split). Returns 0 for invalid arguments too. */
+/* Bytes of device workspace a call with these arguments needs (0 when one CTA
+ * covers all K-chunks of its rows). Returns 0 for invalid arguments too. */
 QMV_API size_t qmv_workspace_size(int M, int N, int K, int bits, int group_size);
 
 /* ------------------------------------------------------------------- run */
@@ -103,8 +105,8 @@ QMV_API size_t qmv_workspace_size(int M, int N, int K, int bits, int group_size)
 /* y = W . x for M vectors, asynchronously on `stream`.
  *
  *  w_q     device, uint32 [N, K*bits/32] from qmv_pack, 16-byte aligned.
- *  scales  device, bf16 bit patterns [N, K/group_size], row-major, 2-byte aligned.
- *  biases  device, bf16 bit patterns [N, K/group_size], row-major, 2-byte aligned.
+ *  scales  device, bf16 bit patterns [N, K/group_size], row-major, 16-byte aligned.
+ *  biases  device, bf16 bit patterns [N, K/group_size], row-major, 16-byte aligned.
  *  x       device, bf16 [M, K], row-major (vector-major), 16-byte aligned.
  *  y       device, bf16 [M, N], row-major; must not overlap any input.
  *  M       1 .. QMV_MAX_M.  N, K >= 1; K a multiple of group_size.
@@ -136,6 +138,12 @@ QMV_API qmv_status qmv_run(const uint32_t *w_q, const uint16_t *scales, const ui
 /* Flags for qmv_run_ex. */
 #define QMV_F32_OUT 0x1u             /* y is float [M, N]: the fp32 value before bf16 rounding */
 #define QMV_FORCE_M1_PER_COLUMN 0x2u /* serve the M vectors as M separate M = 1 launches       */
+/* Launch with a programmatic dependency on the preceding kernel of the stream:
+ * the call may start streaming w_q, scales and biases before that kernel has
+ * finished (x, y and the workspace are touched only after it has). Set it only
+ * when the preceding kernel does not write w_q, scales or biases -- the
+ * decode-loop case, where weights are constant. */
+#define QMV_PDL 0x4u
 
 /* qmv_run with an explicit workspace and flags.
  *
@@ -191,8 +199,10 @@ QMV_API qmv_status qmv_workspace_init(void *workspace, size_t bytes, qmv_stream_
 /* ------------------------------------------------------------ diagnostics */
 
 /* Device-side error word of the current device: kernels set bit 0 when a
- * bounded wait for a weight tile ran out (the output of that launch is then
- * invalid). Synchronizes the device, stores the word in *word and clears it.
+ * bounded wait for a weight tile ran out, bit 1 when a launch shape violated
+ * the shared-memory ring protocol (neither happens with the library's own
+ * launch plans; the output of that launch is then invalid). Synchronizes the
+ * device, stores the word in *word and clears it.
  * Errors: QMV_ERR_NULL, QMV_ERR_CUDA. */
 QMV_API qmv_status qmv_device_error(unsigned *word);
 

@@ -90,7 +90,7 @@ def test_pack_rejects_bad_input(lib):
 
 
 def test_split_plan(lib):
-    # K-chunks of 2048 elements: a function of K and the group size only
+    # K-chunks of 2048 elements: a function of K only
     assert g.qmv_split_count(15360, 3840, 4, 64) == g.qmv_split_count(7, 3840, 4, 64) == 2
     assert g.qmv_split_count(15360, 3840, 2, 64) == 2
     assert g.qmv_split_count(15360, 3840, 2, 128) == 2
@@ -99,16 +99,21 @@ def test_split_plan(lib):
     assert g.qmv_split_count(5120, 17408, 4, 64) == 9
     assert g.qmv_split_count(1, 1000, 4, 64) == 0
     assert g.qmv_workspace_size(1, 256, 1024, 4, 64) == 0
-    # M = 1: x of all of K fits in one CTA's shared memory, so one CTA folds
-    # every chunk of its rows itself and no workspace is needed
+    # one CTA covers all chunks of its rows (no workspace) while the staged x
+    # of all of K fits: M = 1 on both projections, M = 13 on K = 3840
     assert g.qmv_workspace_size(1, 15360, 3840, 4, 64) == 0
-    # M = 13 / 16: one chunk per CTA; chunk values meet in the workspace after
-    # a 256-byte-aligned block of per-tile counters
-    w13 = g.qmv_workspace_size(13, 15360, 3840, 4, 64)
+    assert g.qmv_workspace_size(1, 3840, 15360, 4, 64) == 0
+    assert g.qmv_workspace_size(13, 15360, 3840, 4, 64) == 0
+    # otherwise one chunk per CTA; chunk values meet in the workspace after a
+    # 256-byte-aligned block of one counter per 4-row block
+    NB = 15360 // 4
     w16 = g.qmv_workspace_size(16, 15360, 3840, 4, 64)
-    assert w13 > 2 * 13 * 15360 * 4 and (w13 - 2 * 13 * 15360 * 4) % 256 == 0
-    assert w16 - w13 == 2 * 3 * 15360 * 4
+    assert w16 == (NB * 4 + 255) // 256 * 256 + 2 * 16 * 15360 * 4
+    w13 = g.qmv_workspace_size(13, 3840, 15360, 4, 64)
+    assert w13 == (960 * 4 + 255) // 256 * 256 + 8 * 13 * 3840 * 4
     assert g.qmv_workspace_size(17, 15360, 3840, 4, 64) == 0
+    # sizes whose scale index would pass 2^31 are refused
+    assert g.qmv_split_count(1 << 30, 1 << 13, 4, 64) == 0
 
 
 FAKE = 1 << 20  # an aligned address that validation must reject before any use
@@ -120,6 +125,7 @@ FAKE = 1 << 20  # an aligned address that validation must reject before any use
     (dict(K=1000), 4), (dict(N=0), 4), (dict(K=0), 4),
     (dict(M=0), 5), (dict(M=17), 5),
     (dict(w_q=FAKE + 8), 6), (dict(x=FAKE + 2), 6), (dict(scales=FAKE + 1), 6),
+    (dict(scales=FAKE + 8), 6), (dict(biases=FAKE + 2), 6),
 ])
 def test_run_validation_before_gpu(lib, kw, code):
     args = dict(w_q=FAKE, scales=FAKE, biases=FAKE, x=FAKE, y=FAKE, M=1, N=64, K=1024, bits=4, group_size=64)
@@ -131,6 +137,8 @@ def test_run_validation_before_gpu(lib, kw, code):
 
 def test_run_ex_rejects_flags(lib):
     r = lib.qmv_run_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 64, 1024, 4, 64, None, 0, 0x100, None)
+    assert r == 10
+    r = lib.qmv_run_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 64, 1024, 4, 64, None, 0, 0x8, None)
     assert r == 10
     r = lib.qmv_run_ex(FAKE, FAKE, FAKE, FAKE, FAKE + 2, 1, 64, 1024, 4, 64, None, 0, g.F32_OUT, None)
     assert r == 6

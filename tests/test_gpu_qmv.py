@@ -142,10 +142,11 @@ def test_mutated_order_is_detected(o, tmp_path):
 
 # ----------------------------------------------------------- workspace --
 def test_explicit_workspace_matches_library_workspace():
-    inp = synth.make_inputs(1000, 3840, 13, 4, 64, seed=5)
+    inp = synth.make_inputs(1000, 15360, 13, 4, 64, seed=5)
     dp = DeviceProblem(inp)
     y_lib = dp.run(flags=g.F32_OUT)
-    nbytes = g.qmv_workspace_size(13, 1000, 3840, 4, 64)
+    nbytes = g.qmv_workspace_size(13, 1000, 15360, 4, 64)
+    assert nbytes > 0
     ws = torch.empty(nbytes // 4 + 4, dtype=torch.int32, device="cuda")
     g.qmv_workspace_init(ws, nbytes)
     for _ in range(3):  # the counters return to zero after every call

@@ -28,7 +28,7 @@ def lib():
 
 
 def test_noalloc_matches_existing_entry_point_twice(lib):
-    N, K, M, bits, gs = 15360, 3840, 13, 4, 64
+    N, K, M, bits, gs = 3840, 15360, 13, 4, 64
     need = g.qmv_workspace_size(M, N, K, bits, gs)
     assert 0 < need <= g.NOALLOC_SCRATCH_BYTES  # this problem uses K-split scratch
     inp = synth.make_inputs(N, K, M, bits, gs, seed=41)
