@@ -1,7 +1,7 @@
 // Host side of the C ABI declared in include/qmv.h: argument validation, the
-// launch plan (fixed K-chunks, CTA shape, unit and ring geometry), workspace
-// handling, the scale/bias tensor maps, and dispatch to the kernels (M = 1 ->
-// qmv_m1, M = 2..16 -> qmv_streamed with V = M).
+// launch plans (fixed K-chunks, CTA shape, the one-vector kernel's ring),
+// workspace handling, the scale/bias tensor maps and dispatch to the kernels
+// (M = 1 -> qmv_m1, M = 2..16 -> qmv_streamed with V = M).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -63,24 +63,21 @@ struct Problem {
     int nranges;    // chunk ranges (grid.y)
     int grid_rows;  // CTAs along the rows (grid.x)
     int max_rb;     // row blocks of the largest CTA share
-    int uc;         // chunks per unit
-    int full_rows;  // units are whole rows (one contiguous copy)
-    int pitch;      // bytes per unit row in a ring slot
-    int sb_mode_unit, sbox;
-    int slots, consumers, threads;
+    int threads;
     int smem;       // dynamic shared memory per CTA
+    // one-vector ring
+    int uc, full_rows, pitch, sb_mode_unit, sbox, slots, consumers;
 };
 
 // Largest dynamic shared memory a CTA may use (static shared memory and
 // reserved bytes kept aside).
 constexpr int kSmemBudget = 227 * 1024 - 512;
-// Staged x of one CTA at most (the rest of shared memory feeds the weight ring).
-constexpr int kXsBudget = 112 * 1024;
-// Largest unit (4 rows of weights) and ring depth.
-constexpr int kUnitMax = 12 * 1024;
-constexpr int kMaxSlots = 24;
 // Chunk values of one CTA at most (bounds its share of rows).
-constexpr int kCvBudget = 32 * 1024;
+constexpr int kCvBudget = 16 * 1024;
+// One-vector kernel: staged x at most, largest unit, ring depth.
+constexpr int kXsBudgetV1 = 100 * 1024;
+constexpr int kUnitMax = 8 * 1024;
+constexpr int kMaxSlots = 24;
 
 #if defined(QMV_TUNING)
 // Tuning builds only: fixed launch shapes for sweeps (0 = automatic).
@@ -88,42 +85,24 @@ struct TuneOverride { int slots = 0, uc = 0, consumers = 0, grid_rows = 0, cpc =
 TuneOverride g_tune;
 #endif
 
-int xs_bytes(int V, int nsub) { return V == 1 ? nsub * qmv::kXsF32 * 4 : V * nsub * qmv::kXsB16; }
-
-// Launch shape of a call. `sms` is the device's SM count, or 0 when unknown.
-// Whether a workspace is needed, and its size, never depend on `sms`, so
-// qmv_workspace_size can be answered without a GPU.
-Problem plan(int V, int N, int K, int bits, int gs, int sms)
+void common_shape(Problem &pr, int V, int N, int K, int bits, int gs)
 {
-    Problem pr{};
     pr.V = V; pr.N = N; pr.K = K; pr.bits = bits; pr.gs = gs;
     pr.G = K / gs;
     pr.S_row = qmv::subs_per_row(K);
     pr.ks = qmv::chunk_count(K);
     pr.row_bytes = int((long long)K * bits / 8);
     pr.NB = (N + qmv::kRows - 1) / qmv::kRows;
-    pr.consumers = qmv::consumer_warps(V);
-    pr.threads = 32 * (pr.consumers + qmv::producer_warps(V));
-    // Chunks per CTA: all of K when the staged x of all of K fits, else as many
-    // as fit (one for the streamed kernel).
-    const int per_chunk = xs_bytes(V, qmv::kChunkSubs);
-    if (xs_bytes(V, pr.S_row) <= kXsBudget)
-        pr.cpc = pr.ks;
-    else
-        pr.cpc = V == 1 ? kXsBudget / per_chunk : 1;
-#if defined(QMV_TUNING)
-    if (g_tune.cpc > 0 && g_tune.cpc <= pr.ks) pr.cpc = g_tune.cpc;
-    if (g_tune.consumers > 0 && g_tune.consumers <= qmv::consumer_warps(V)) {
-        pr.consumers = g_tune.consumers;
-        pr.threads = 32 * (pr.consumers + qmv::producer_warps(V));
-    }
-#endif
+}
+
+// A persistent grid of about one CTA per SM: the chunk ranges times an even
+// split of the row blocks; more CTAs (several waves) when a share of rows
+// would exceed the chunk-value cap.
+void grid_shape(Problem &pr, int sms, int V)
+{
     pr.nranges = (pr.ks + pr.cpc - 1) / pr.cpc;
-    // A persistent grid of about one CTA per SM: the chunk ranges times an
-    // even split of the row blocks.
     int gr = sms > 0 ? sms / pr.nranges : 1;
     if (gr < 1) gr = 1;
-    // more CTAs (several waves) when a share of rows would not fit its chunk values
     const int rb_cap = kCvBudget / (qmv::kRows * pr.cpc * V * 4) > 0 ? kCvBudget / (qmv::kRows * pr.cpc * V * 4) : 1;
     if ((pr.NB + gr - 1) / gr > rb_cap) gr = (pr.NB + rb_cap - 1) / rb_cap;
     if (gr > pr.NB) gr = pr.NB;
@@ -132,8 +111,50 @@ Problem plan(int V, int N, int K, int bits, int gs, int sms)
 #endif
     pr.grid_rows = gr;
     pr.max_rb = (pr.NB + gr - 1) / gr;
-    // Units: whole rows in one contiguous copy when the CTA covers all of K and
-    // four rows are small enough; otherwise uc chunks of each row.
+}
+
+// Streamed kernel (V >= 2): all of K per CTA (no workspace) when the staged
+// x fits, else the widest chunk range that fits (one chunk always does).
+// Whether a workspace is needed never depends on `sms` (the fit is checked
+// against the chunk-value cap), so qmv_workspace_size needs no GPU.
+Problem plan_direct(int V, int N, int K, int bits, int gs, int sms)
+{
+    Problem pr{};
+    common_shape(pr, V, N, K, bits, gs);
+    const int warps = qmv::kStreamedWarps;
+    const int wbuf = qmv::vectors_per_pass(V) < V ? warps * qmv::kRows * 32 * qmv::sub_bytes(bits) : 0;
+    auto fits = [&](int cpc) {
+        const int nsub = cpc * qmv::kChunkSubs < pr.S_row ? cpc * qmv::kChunkSubs : pr.S_row;
+        return qmv::align_up(V * nsub * qmv::kXsB16, 16) + kCvBudget + wbuf + 16 + 128 <= kSmemBudget;
+    };
+    pr.cpc = pr.ks;
+    while (pr.cpc > 1 && !fits(pr.cpc)) --pr.cpc;
+#if defined(QMV_TUNING)
+    if (g_tune.cpc > 0 && g_tune.cpc <= pr.ks) pr.cpc = g_tune.cpc;
+#endif
+    pr.threads = 32 * warps;
+    grid_shape(pr, sms, V);
+    const int nsub = pr.cpc * qmv::kChunkSubs < pr.S_row ? pr.cpc * qmv::kChunkSubs : pr.S_row;
+    pr.smem = qmv::smem_layout(bits, V, warps, nsub, pr.max_rb, pr.cpc).total;
+    return pr;
+}
+
+// One-vector kernel: chunks per CTA from the staged-x budget (all of K when
+// it fits), units (whole rows in one copy when four rows fit kUnitMax, else
+// uc chunks of each row), scale/bias boxes, then as many ring slots as fit
+// (a multiple of the producer warps, at most kMaxSlots and the CTA's units).
+Problem plan_ring(int N, int K, int bits, int gs, int sms)
+{
+    Problem pr{};
+    common_shape(pr, 1, N, K, bits, gs);
+    const int per_chunk = qmv::kChunkSubs * qmv::kXsF32 * 4;
+    pr.cpc = pr.S_row * qmv::kXsF32 * 4 <= kXsBudgetV1 ? pr.ks : kXsBudgetV1 / per_chunk;
+    pr.consumers = qmv::kRingConsumers;
+#if defined(QMV_TUNING)
+    if (g_tune.cpc > 0 && g_tune.cpc <= pr.ks) pr.cpc = g_tune.cpc;
+    if (g_tune.consumers > 0 && g_tune.consumers <= qmv::kRingConsumers) pr.consumers = g_tune.consumers;
+#endif
+    grid_shape(pr, sms, 1);
     const int cb = qmv::chunk_bytes(bits);
     if (pr.cpc == pr.ks && qmv::kRows * pr.row_bytes <= kUnitMax) {
         pr.full_rows = 1;
@@ -162,30 +183,27 @@ Problem plan(int V, int N, int K, int bits, int gs, int sms)
     }
     const int nsub = pr.cpc * qmv::kChunkSubs < pr.S_row ? pr.cpc * qmv::kChunkSubs : pr.S_row;
     auto layout = [&](int slots) {
-        return qmv::smem_layout(bits, V, pr.pitch, pr.sb_mode_unit, pr.sbox, slots, nsub, pr.max_rb, pr.cpc);
+        return qmv::ring_layout(pr.pitch, pr.sb_mode_unit, pr.sbox, slots, nsub, pr.max_rb, pr.cpc);
     };
-    // Ring depth: as many slots as fit, but no more than the units of a CTA.
     const int upr = (pr.cpc + pr.uc - 1) / pr.uc;
     const int units = pr.max_rb * upr;
     int slots = kMaxSlots < units ? kMaxSlots : units;
-    if (slots < 2) slots = 2;
 #if defined(QMV_TUNING)
     if (g_tune.slots >= 2) slots = g_tune.slots;
 #endif
-    // every slot is served by one producer: a multiple of the producer count
-    const int P = qmv::producer_warps(V);
+    const int P = qmv::kRingProducers;
     slots = (slots + P - 1) / P * P;
     while (slots > P && layout(slots).total > kSmemBudget) slots -= P;
     pr.slots = slots;
     pr.smem = layout(slots).total;
-    // A consumer waits on a slot's "full" barrier by phase parity, which is
-    // only unambiguous while no consumer can run two laps of the ring ahead of
-    // the producer: at most one consumer warp per slot.
-    if (pr.consumers > pr.slots) {
-        pr.consumers = pr.slots;
-        pr.threads = 32 * (pr.consumers + P);
-    }
+    if (pr.consumers > pr.slots) pr.consumers = pr.slots;  // at most one consumer warp per slot
+    pr.threads = 32 * (pr.consumers + P);
     return pr;
+}
+
+Problem plan(int V, int N, int K, int bits, int gs, int sms)
+{
+    return V == 1 ? plan_ring(N, K, bits, gs, sms) : plan_direct(V, N, K, bits, gs, sms);
 }
 
 size_t counter_bytes(int NB) { return (size_t(NB) * sizeof(unsigned) + 255) & ~size_t(255); }
@@ -280,7 +298,7 @@ qmv_status library_workspace(int dev, size_t need, void **out)
     return QMV_OK;
 }
 
-cudaError_t dispatch(const Problem &pr, const CUtensorMap &map_s, const CUtensorMap &map_b, const qmv::Params &p,
+cudaError_t dispatch(const Problem &pr, const CUtensorMap *map_s, const CUtensorMap *map_b, const qmv::Params &p,
                      bool pdl, cudaStream_t stream)
 {
     qmv::Launch l;
@@ -288,10 +306,20 @@ cudaError_t dispatch(const Problem &pr, const CUtensorMap &map_s, const CUtensor
     l.threads = pr.threads;
     l.smem = size_t(pr.smem);
     l.pdl = pdl;
-    if (pr.bits == 4 && pr.gs == 64) return qmv::launch_b4g64(pr.V, map_s, map_b, p, l, stream);
-    if (pr.bits == 4 && pr.gs == 128) return qmv::launch_b4g128(pr.V, map_s, map_b, p, l, stream);
-    if (pr.bits == 2 && pr.gs == 64) return qmv::launch_b2g64(pr.V, map_s, map_b, p, l, stream);
-    return qmv::launch_b2g128(pr.V, map_s, map_b, p, l, stream);
+    if (pr.V == 1) {
+        qmv::RingParams rp;
+        static_cast<qmv::Params &>(rp) = p;
+        rp.uc = pr.uc; rp.full_rows = pr.full_rows; rp.pitch = pr.pitch; rp.sb_mode_unit = pr.sb_mode_unit;
+        rp.sbox = pr.sbox; rp.slots = pr.slots; rp.consumers = pr.consumers;
+        if (pr.bits == 4 && pr.gs == 64) return qmv::launch_b4g64_m1(*map_s, *map_b, rp, l, stream);
+        if (pr.bits == 4 && pr.gs == 128) return qmv::launch_b4g128_m1(*map_s, *map_b, rp, l, stream);
+        if (pr.bits == 2 && pr.gs == 64) return qmv::launch_b2g64_m1(*map_s, *map_b, rp, l, stream);
+        return qmv::launch_b2g128_m1(*map_s, *map_b, rp, l, stream);
+    }
+    if (pr.bits == 4 && pr.gs == 64) return qmv::launch_b4g64_streamed(pr.V, p, l, stream);
+    if (pr.bits == 4 && pr.gs == 128) return qmv::launch_b4g128_streamed(pr.V, p, l, stream);
+    if (pr.bits == 2 && pr.gs == 64) return qmv::launch_b2g64_streamed(pr.V, p, l, stream);
+    return qmv::launch_b2g128_streamed(pr.V, p, l, stream);
 }
 
 qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t *biases, const uint16_t *x, void *y,
@@ -331,26 +359,29 @@ qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t 
             if (st != QMV_OK) return st;
         }
     }
+
     unsigned *err = nullptr;
     st = device_error_ptr(dev, &err);
     if (st != QMV_OK) return st;
 
     CUtensorMap map_s, map_b;
-    int enc = encode_sb_map(&map_s, scales, pr);
-    if (enc == 0) enc = encode_sb_map(&map_b, biases, pr);
-    if (enc != 0) {
-        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled(scales/biases) returned %d%s", enc,
-                 enc < 0 ? " (driver entry point not found)" : "");
-        return QMV_ERR_CUDA;
+    if (V == 1) {
+        int enc = encode_sb_map(&map_s, scales, pr);
+        if (enc == 0) enc = encode_sb_map(&map_b, biases, pr);
+        if (enc != 0) {
+            snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled(scales/biases) returned %d%s", enc,
+                     enc < 0 ? " (driver entry point not found)" : "");
+            return QMV_ERR_CUDA;
+        }
     }
 
     qmv::Params p;
-    p.w = reinterpret_cast<const uint8_t *>(w_q);
     p.err = err;
+    p.w = reinterpret_cast<const uint8_t *>(w_q);
+    p.scales = scales;
+    p.biases = biases;
     p.N = N; p.K = K; p.G = pr.G; p.S_row = pr.S_row; p.ks = pr.ks; p.row_bytes = pr.row_bytes;
-    p.NB = pr.NB; p.grid_rows = pr.grid_rows; p.cpc = pr.cpc; p.uc = pr.uc; p.full_rows = pr.full_rows;
-    p.pitch = pr.pitch; p.sb_mode_unit = pr.sb_mode_unit; p.sbox = pr.sbox; p.slots = pr.slots;
-    p.consumers = pr.consumers; p.max_rb = pr.max_rb;
+    p.NB = pr.NB; p.grid_rows = pr.grid_rows; p.cpc = pr.cpc; p.max_rb = pr.max_rb;
     p.f32_out = f32_out ? 1 : 0;
     p.counters = need ? static_cast<unsigned *>(workspace) : nullptr;
     p.partials = need ? reinterpret_cast<float *>(static_cast<char *>(workspace) + counter_bytes(pr.NB)) : nullptr;
@@ -361,7 +392,7 @@ qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t 
     for (int m = 0; m < launches; ++m) {
         p.x = x + size_t(m) * K;
         p.y = static_cast<char *>(y) + size_t(m) * N * ysize;
-        ce = dispatch(pr, map_s, map_b, p, pdl, stream);
+        ce = dispatch(pr, &map_s, &map_b, p, pdl, stream);
         if (ce != cudaSuccess) return cuda_fail("kernel launch", ce);
     }
     return QMV_OK;

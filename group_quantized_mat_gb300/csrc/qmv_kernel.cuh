@@ -17,7 +17,7 @@
 //     q_i << (bits*k_i) -- the subnormal q_i * 2^(bits*k_i - 149) -- so every
 //     product equals q_i * x_i * 2^(105 - E) exactly (for all x_i down to
 //     2^-120 times the subgroup's largest). Two running sums a_e, a_o over the
-//     even and odd elements, in processing order from +0, one packed
+//     even and odd elements in processing order from +0, one packed
 //     fma.rn.f32x2 per element pair; d = ((a_e + a_o) * f1) * f2 with
 //     f1 * f2 = 2^(E - 105);
 //  2. term = fma(s_g, d, b_g * sx), sx = sum of the subgroup's 64 x: eight
@@ -30,15 +30,21 @@
 //  5. one rounding to bf16, nearest even.
 // Processing order inside a 4-bit subgroup: its two 16-byte halves, the half
 // selected by bit 2 of the subgroup index first (that keeps the eight lanes of
-// a shared-memory phase on distinct banks); inside a half, increasing element
-// order. 2-bit subgroups run in increasing element order.
+// a shared-memory phase on distinct banks when a warp reads 32 subgroups of a
+// row); inside a half, increasing element order. 2-bit subgroups run in
+// increasing element order.
 //
 // Work decomposition (none of it changes the arithmetic): a unit is 4 rows x
-// uc chunks; lane l of the warp processing a unit owns subgroup l of each of
-// its chunks in all 4 rows. One producer warp streams units into a ring of
-// shared-memory slots (1-D bulk copies of the weight rows, 1-D tensor-map boxes
-// of scales and biases, one mbarrier per slot for "full" and one for "empty");
-// consumer warps take units in order from a shared counter.
+// some chunks; lane l of the warp processing a unit owns subgroup l of each
+// of its chunks in all 4 rows. Warps take units from a shared counter.
+//  * qmv_m1 (one vector): producer warps stream units (4 whole rows in one
+//    1-D bulk copy when they fit, else the rows' chunks, plus 1-D tensor-map
+//    boxes of the rows' scales and biases) into a CTA-wide ring of
+//    shared-memory slots, one "full" and one "empty" mbarrier per slot;
+//    consumer warps compute them.
+//  * qmv_streamed (V vectors): a warp loads its unit's bytes (the lane's own
+//    subgroup of 4 rows of one chunk), scales and biases straight into
+//    registers; V times the arithmetic hides the latency.
 #pragma once
 
 #include <cuda.h>
@@ -66,6 +72,11 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 __device__ __forceinline__ void fence_mbar_init()
 {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
@@ -183,6 +194,12 @@ __device__ __forceinline__ uint4 lds_v4_u32(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ void sts_v4_u32(uint32_t addr, const uint4 &v)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 __device__ __forceinline__ float4 lds_f4(uint32_t addr)
 {
     float4 v;
@@ -254,8 +271,8 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &c, int k)
 }
 
 // Pairs of octet `o` (0..7 in processing order) of a subgroup, for BITS.
-// quads[p] = the subgroup's p-th 16-byte piece as loaded (4-bit: two pieces,
-// processing order; 2-bit: one piece).
+// quads[p] = the subgroup's 16-byte pieces in processing order (4-bit: two
+// pieces; 2-bit: one).
 template <int BITS>
 __device__ __forceinline__ void subgroup_octet(const uint4 (&quads)[BITS == 4 ? 2 : 1], int o, uint64_t (&q)[4])
 {
@@ -268,8 +285,8 @@ __device__ __forceinline__ void subgroup_octet(const uint4 (&quads)[BITS == 4 ? 
     }
 }
 
-// Byte offsets, inside one row of a slot, of the lane's subgroup pieces in
-// processing order (4-bit: the half selected by bit 2 of the subgroup first).
+// Byte offsets, inside a row's copy of a chunk, of the lane's subgroup pieces
+// in processing order (4-bit: the half selected by bit 2 of the lane first).
 template <int BITS>
 __device__ __forceinline__ void piece_offsets(int lane, uint32_t (&off)[BITS == 4 ? 2 : 1])
 {
@@ -283,18 +300,12 @@ __device__ __forceinline__ void piece_offsets(int lane, uint32_t (&off)[BITS == 
 }
 
 // Step 1 for V = 1: acc[r] = (a_e, a_o) of the lane's subgroup in rows 0..3.
-//   wrow[r]  shared address of row r's subgroup bytes (piece offsets added);
-//   xsub     shared address of the staged subgroup (64 fp32 x' in processing order).
+//   quads[r]  the subgroup's bytes in row r (16-byte pieces, processing order);
+//   xsub      shared address of the staged subgroup (64 fp32 x').
 template <int BITS>
-__device__ __forceinline__ void subgroup_dot_v1(const uint32_t (&wrow)[kRows][BITS == 4 ? 2 : 1], uint32_t xsub,
+__device__ __forceinline__ void subgroup_dot_v1(const uint4 (&quads)[kRows][BITS == 4 ? 2 : 1], uint32_t xsub,
                                                 uint64_t (&acc)[kRows])
 {
-    constexpr int NP = BITS == 4 ? 2 : 1;
-    uint4 quads[kRows][NP];
-#pragma unroll
-    for (int r = 0; r < kRows; ++r)
-#pragma unroll
-        for (int pc = 0; pc < NP; ++pc) quads[r][pc] = lds_v4_u32(wrow[r][pc]);
 #pragma unroll
     for (int r = 0; r < kRows; ++r) acc[r] = 0ull;
 #pragma unroll
@@ -317,15 +328,9 @@ __device__ __forceinline__ void subgroup_dot_v1(const uint32_t (&wrow)[kRows][BI
 // Step 1 for VP vectors from bf16-staged x': acc[r][v].
 //   xsub   shared address of vector 0's staged subgroup; xv bytes between vectors.
 template <int BITS, int VP>
-__device__ __forceinline__ void subgroup_dot_vp(const uint32_t (&wrow)[kRows][BITS == 4 ? 2 : 1], uint32_t xsub,
+__device__ __forceinline__ void subgroup_dot_vp(const uint4 (&quads)[kRows][BITS == 4 ? 2 : 1], uint32_t xsub,
                                                 uint32_t xv, uint64_t (&acc)[kRows][VP])
 {
-    constexpr int NP = BITS == 4 ? 2 : 1;
-    uint4 quads[kRows][NP];
-#pragma unroll
-    for (int r = 0; r < kRows; ++r)
-#pragma unroll
-        for (int pc = 0; pc < NP; ++pc) quads[r][pc] = lds_v4_u32(wrow[r][pc]);
 #pragma unroll
     for (int r = 0; r < kRows; ++r)
 #pragma unroll
@@ -351,6 +356,21 @@ __device__ __forceinline__ void subgroup_dot_vp(const uint32_t (&wrow)[kRows][BI
             }
         }
     }
+}
+
+// subgroup_dot_vp with the weight bytes re-read from shared memory (cell
+// (r, pc) of this lane at wcell + (r*NP + pc) * 512), for two-pass V.
+template <int BITS, int VP>
+__device__ __forceinline__ void subgroup_dot_vp_smem(uint32_t wcell, uint32_t xsub, uint32_t xv,
+                                                     uint64_t (&acc)[kRows][VP])
+{
+    constexpr int NP = BITS == 4 ? 2 : 1;
+    uint4 quads[kRows][NP];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r)
+#pragma unroll
+        for (int pc = 0; pc < NP; ++pc) quads[r][pc] = lds_v4_u32(wcell + uint32_t(r * NP + pc) * 512u);
+    subgroup_dot_vp<BITS, VP>(quads, xsub, xv, acc);
 }
 
 // Step 2: the subgroup's term from its pair sums.
@@ -402,27 +422,188 @@ __device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(_
 
 template <int BITS, int V>
 struct Traits {
-    static constexpr int VP = V <= 8 ? V : (V + 1) / 2;       // vectors per pass
+    static constexpr int VP = vectors_per_pass(V);
     static constexpr int PASSES = (V + VP - 1) / VP;
     static constexpr int NVAL = kRows * VP;
     static constexpr int NRED = NVAL <= 4 ? 4 : NVAL <= 8 ? 8 : NVAL <= 16 ? 16 : 32;
     static constexpr int NP = BITS == 4 ? 2 : 1;              // 16-byte pieces per subgroup row
 };
 
-template <int BITS, int GS, int V>
-__device__ __forceinline__ void qmv_body(const CUtensorMap *map_s, const CUtensorMap *map_b, const Params &p)
+// Stages x of subgroups [sub_lo, sub_lo + nsub) of every vector at smem + xs_off
+// (steps 1 and 2 of the fixed order): eight threads per subgroup, eight
+// elements each; threads [0, nthreads) of the CTA take part.
+template <int BITS, int V>
+__device__ __forceinline__ void stage_x(uint8_t *smem, int xs_off, const uint16_t *x, int K, int sub_lo, int nsub,
+                                        int nsub_max, int tid, int nthreads)
 {
-    using T = Traits<BITS, V>;
+    const int per_vec = nsub * 8, all = V * per_vec;
+    const int all_pad = (all + nthreads - 1) / nthreads * nthreads;
+    for (int u = tid; u < all_pad; u += nthreads) {
+        const bool live = u < all;
+        const int v = live ? u / per_vec : 0;
+        const int rem = live ? u - v * per_vec : 0;
+        const int sl = rem >> 3, e8 = rem & 7;  // subgroup (CTA-local), eighth
+        uint4 raw = make_uint4(0, 0, 0, 0);
+        if (live) raw = __ldg(reinterpret_cast<const uint4 *>(x + size_t(v) * K + size_t(sub_lo + sl) * kSub) + e8);
+        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint32_t e = 1;
+        float xv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t bits = (i & 1) ? (w4[i / 2] >> 16) : (w4[i / 2] & 0xFFFFu);
+            xv[i] = bf16_bits_to_f32(bits);
+            const uint32_t f = (bits >> 7) & 0xFFu;
+            e = f > e ? f : e;
+        }
+        // largest exponent field of the subgroup (its eight threads are eight consecutive lanes)
+#pragma unroll
+        for (int m = 1; m < 8; m <<= 1) {
+            const uint32_t o = __shfl_xor_sync(0xffffffffu, e, m);
+            e = o > e ? o : e;
+        }
+        // x' = x * 2^(254 - bits*k - E), as two exact power-of-two factors
+        float xr[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int k = BITS == 4 ? (i & 3) : i;
+            const int pw = 254 - BITS * k - int(e);
+            const int p1 = pw < 127 ? pw : 127;
+            const float m1 = __uint_as_float(uint32_t(p1 + 127) << 23);
+            const float m2 = __uint_as_float(uint32_t(pw - p1 + 127) << 23);
+            xr[i] = bf16_round(__fmul_rn(__fmul_rn(xv[i], m1), m2));
+        }
+        // eight-element sum, left to right; the subgroup's sum gathers the eight in order
+        float s8 = xv[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) s8 = __fadd_rn(s8, xv[i]);
+        float sx = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float o = __shfl_sync(0xffffffffu, s8, i, 8);
+            sx = i == 0 ? o : __fadd_rn(sx, o);
+        }
+        if (live) {
+            // octet position of these eight elements in processing order
+            const int t = sub_lo + sl;
+            const int oct = BITS == 4 ? (e8 ^ (((t >> 2) & 1) * 4)) : e8;
+            if constexpr (V == 1) {
+                float4 *dst = reinterpret_cast<float4 *>(smem + xs_off + size_t(sl) * kXsF32 * 4 + oct * 32);
+                dst[0] = make_float4(xr[0], xr[1], xr[2], xr[3]);
+                dst[1] = make_float4(xr[4], xr[5], xr[6], xr[7]);
+            } else {
+                uint32_t pk[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    pk[i] = (__float_as_uint(xr[2 * i]) >> 16) | (__float_as_uint(xr[2 * i + 1]) & 0xFFFF0000u);
+                *reinterpret_cast<uint4 *>(smem + xs_off + (size_t(v) * nsub_max + sl) * kXsB16 + oct * 16) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            if (e8 == 0) {
+                const int c = int(e) - 105;  // f1 * f2 = 2^c
+                const int c1 = c < 127 ? c : 127;
+                const float4 meta = make_float4(sx, __uint_as_float(uint32_t(c1 + 127) << 23),
+                                                __uint_as_float(uint32_t(c - c1 + 127) << 23), 0.0f);
+                if constexpr (V == 1)
+                    *reinterpret_cast<float4 *>(smem + xs_off + size_t(sl) * kXsF32 * 4 + 256) = meta;
+                else
+                    *reinterpret_cast<float4 *>(smem + xs_off + (size_t(v) * nsub_max + sl) * kXsB16 + 128) = meta;
+            }
+        }
+    }
+}
+
+// One chunk of one vector for 4 rows (steps 1 to 3): the lane's subgroup
+// from `quads`, x' of subgroup `sl` at xsub; returns the chunk value of row
+// lane >> 3 (all lanes of that row's eight-lane group hold it).
+template <int BITS>
+__device__ __forceinline__ float chunk_v1(const uint4 (&quads)[kRows][BITS == 4 ? 2 : 1], uint32_t xsub,
+                                          const float (&fs)[kRows], const float (&fb)[kRows], bool active, int lane)
+{
+    uint64_t acc[kRows];
+    subgroup_dot_v1<BITS>(quads, xsub, acc);
+    const float4 meta = lds_f4(xsub + 256);
+    float val[4];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+        const float term = subgroup_term<false>(acc[r], fs[r], fb[r], meta.x, meta.y, meta.z);
+        val[r] = active ? term : 0.0f;
+    }
+    return tree_reduce_scatter<4>(val, lane);
+}
+
+// Step 4 and the output: fold the chunk values of the CTA's rows (cvs, laid
+// out [row][chunk][vector]) left to right into y -- directly when the CTA
+// covers all chunks, else through the workspace, the CTA that completes a row
+// range last folding all chunks (and zeroing what it read, so the workspace
+// is zero again).
+template <int V>
+__device__ __forceinline__ void fold_chunks(const float *cvs, int nrows, int row_t0, int c_lo, int cpc_here, int rb_lo,
+                                            int tid, int nthreads, int N, int ks, int cpc, float *partials,
+                                            unsigned *counters, void *y, int f32_out)
+{
+    __shared__ unsigned s_ticket;
+    auto store_y = [&](int v, int n, float val) {
+        if (f32_out)
+            static_cast<float *>(y)[size_t(v) * N + n] = val;
+        else
+            static_cast<__nv_bfloat16 *>(y)[size_t(v) * N + n] = __float2bfloat16_rn(val);
+    };
+    if (cpc >= ks) {
+        for (int idx = tid; idx < nrows * V; idx += nthreads) {
+            const int v = idx / nrows, r = idx - v * nrows;
+            const int n = row_t0 + r;
+            if (n >= N) continue;
+            float acc = cvs[(r * cpc_here) * V + v];
+            for (int c = 1; c < ks; ++c) acc = __fadd_rn(acc, cvs[(r * cpc_here + c) * V + v]);
+            store_y(v, n, acc);
+        }
+        return;
+    }
+    for (int idx = tid; idx < nrows * V * cpc_here; idx += nthreads) {
+        const int cl = idx / (nrows * V), rem = idx - cl * nrows * V;
+        const int v = rem / nrows, r = rem - v * nrows;
+        const int n = row_t0 + r;
+        if (n < N) __stcg(partials + (size_t(c_lo + cl) * V + v) * N + n, cvs[(r * cpc_here + cl) * V + v]);
+    }
+    __threadfence();
+    __syncthreads();
+    const unsigned nranges = unsigned(gridDim.y);
+    if (tid == 0) s_ticket = atomicInc(counters + rb_lo, nranges - 1);
+    __syncthreads();
+    if (s_ticket != nranges - 1) return;
+    __threadfence();
+    for (int idx = tid; idx < nrows * V; idx += nthreads) {
+        const int v = idx / nrows, r = idx - v * nrows;
+        const int n = row_t0 + r;
+        if (n >= N) continue;
+        float *pp = partials + size_t(v) * N + n;
+        float acc = __ldcg(pp);
+        __stcg(pp, 0.0f);
+        for (int c = 1; c < ks; ++c) {
+            float *pc = pp + size_t(c) * V * N;
+            acc = __fadd_rn(acc, __ldcg(pc));
+            __stcg(pc, 0.0f);
+        }
+        store_y(v, n, acc);
+    }
+}
+
+// ------------------------------------------------------- one vector: ring --
+
+template <int BITS, int GS>
+__device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_s, const CUtensorMap *map_b, const RingParams &p)
+{
     constexpr int kSubB = sub_bytes(BITS);
     constexpr int kChunkB = chunk_bytes(BITS);
+    constexpr int NP = BITS == 4 ? 2 : 1;
 
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    __shared__ unsigned s_ticket;
     uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nthreads = blockDim.x, nwarps = nthreads >> 5;
     const int C = p.consumers;
+    const int P = nwarps - C;
 
     const int c_lo = blockIdx.y * p.cpc;
     const int c_hi = c_lo + p.cpc < p.ks ? c_lo + p.cpc : p.ks;
@@ -432,12 +613,12 @@ __device__ __forceinline__ void qmv_body(const CUtensorMap *map_s, const CUtenso
     const int rb_lo = int((long long)blockIdx.x * p.NB / p.grid_rows);
     const int rb_hi = int((long long)(blockIdx.x + 1) * p.NB / p.grid_rows);
     const int row_t0 = rb_lo * kRows;
-    const int upr = (c_hi - c_lo + p.uc - 1) / p.uc;  // units per row block
-    const int nunits = (rb_hi - rb_lo) * upr;
     const int cpc_here = c_hi - c_lo;
+    const int upr = (cpc_here + p.uc - 1) / p.uc;  // units per row block
+    const int nunits = (rb_hi - rb_lo) * upr;
 
     const int nsub_max = p.cpc * kChunkSubs < p.S_row ? p.cpc * kChunkSubs : p.S_row;
-    const SmemLayout L = smem_layout(BITS, V, p.pitch, p.sb_mode_unit, p.sbox, p.slots, nsub_max, p.max_rb, p.cpc);
+    const RingLayout L = ring_layout(p.pitch, p.sb_mode_unit, p.sbox, p.slots, nsub_max, p.max_rb, p.cpc);
     const uint32_t ring = smem_u32(smem + L.ring);
     const uint32_t xs = smem_u32(smem + L.xs);
     float *cvs = reinterpret_cast<float *>(smem + L.cv);
@@ -448,7 +629,7 @@ __device__ __forceinline__ void qmv_body(const CUtensorMap *map_s, const CUtenso
     volatile int *s_issued = reinterpret_cast<volatile int *>(s_next + 2);
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + p.slots);
 
-    // Geometry of unit u: rows [r0, r0 + 4), chunks [c0, c1).
+    // Geometry of unit u: rows [r0, r0 + nr), chunks [c0, c1).
     struct Unit {
         int r0, nr, c0, c1;
     };
@@ -464,7 +645,7 @@ __device__ __forceinline__ void qmv_body(const CUtensorMap *map_s, const CUtenso
     // Element coordinate of scale/bias box `bx` of a unit (rows r0.., groups from chunk c0).
     auto sb_coord = [&](const Unit &g, int bx) {
         const long long g0 = (long long)g.c0 * kChunkElems / GS;
-        return round_down8((long long)(g.r0 + bx) * p.G + g0);
+        return int(((long long)(g.r0 + bx) * p.G + g0) & ~7ll);
     };
 
     const uint64_t pol = l2_evict_first_policy();
@@ -491,9 +672,8 @@ __device__ __forceinline__ void qmv_body(const CUtensorMap *map_s, const CUtenso
         }
     };
 
-    // The ring protocol needs at most one consumer warp per slot and every
-    // slot served by one producer (slots a multiple of the producer count).
-    const int P = nwarps - C;
+    // The ring protocol needs every slot served by one producer (slots a
+    // multiple of the producer count) and at most one consumer per slot.
     if (C > p.slots || C < 1 || P < 1 || p.slots % P != 0) {
         if (tid == 0) atomicOr(p.err, 2u);
         return;
@@ -555,95 +735,13 @@ __device__ __forceinline__ void qmv_body(const CUtensorMap *map_s, const CUtenso
             *s_abort = 1;
         }
     } else {
-        // x may be written by the preceding grid: wait for it.
-        grid_dependency_wait();
-        // Stage x of subgroups [sub_lo, sub_hi) for every vector: eight threads
-        // per subgroup, eight elements each (steps 1 and 2 of the fixed order).
-        {
-            const int per_vec = nsub * 8, all = V * per_vec;
-            const int nct = C * 32;  // consumer threads
-            const int all_pad = (all + nct - 1) / nct * nct;
-            for (int u = tid; u < all_pad; u += nct) {
-                const bool live = u < all;
-                const int v = live ? u / per_vec : 0;
-                const int rem = live ? u - v * per_vec : 0;
-                const int sl = rem >> 3, e8 = rem & 7;  // subgroup (CTA-local), eighth
-                uint4 raw = make_uint4(0, 0, 0, 0);
-                if (live)
-                    raw = __ldg(reinterpret_cast<const uint4 *>(p.x + size_t(v) * p.K + size_t(sub_lo + sl) * kSub) + e8);
-                const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-                uint32_t e = 1;
-                float xv[8];
-    #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t bits = (i & 1) ? (w4[i / 2] >> 16) : (w4[i / 2] & 0xFFFFu);
-                    xv[i] = bf16_bits_to_f32(bits);
-                    const uint32_t f = (bits >> 7) & 0xFFu;
-                    e = f > e ? f : e;
-                }
-                // largest exponent field of the subgroup (its eight threads are eight consecutive lanes)
-    #pragma unroll
-                for (int m = 1; m < 8; m <<= 1) {
-                    const uint32_t o = __shfl_xor_sync(0xffffffffu, e, m);
-                    e = o > e ? o : e;
-                }
-                // x' = x * 2^(254 - bits*k - E), as two exact power-of-two factors
-                float xr[8];
-    #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int k = BITS == 4 ? (i & 3) : i;
-                    const int pw = 254 - BITS * k - int(e);
-                    const int p1 = pw < 127 ? pw : 127;
-                    const float m1 = __uint_as_float(uint32_t(p1 + 127) << 23);
-                    const float m2 = __uint_as_float(uint32_t(pw - p1 + 127) << 23);
-                    xr[i] = bf16_round(__fmul_rn(__fmul_rn(xv[i], m1), m2));
-                }
-                // eight-element sum, left to right; the subgroup's sum gathers the eight in order
-                float s8 = xv[0];
-    #pragma unroll
-                for (int i = 1; i < 8; ++i) s8 = __fadd_rn(s8, xv[i]);
-                float sx = 0.0f;
-    #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float o = __shfl_sync(0xffffffffu, s8, i, 8);
-                    sx = i == 0 ? o : __fadd_rn(sx, o);
-                }
-                if (live) {
-                    const int t = sub_lo + sl;  // subgroup index in the row
-                    // octet position of these eight elements in processing order
-                    const int oct = BITS == 4 ? (e8 ^ (((t >> 2) & 1) * 4)) : e8;
-                    if constexpr (V == 1) {
-                        float4 *dst = reinterpret_cast<float4 *>(smem + L.xs + size_t(sl) * kXsF32 * 4 + oct * 32);
-                        dst[0] = make_float4(xr[0], xr[1], xr[2], xr[3]);
-                        dst[1] = make_float4(xr[4], xr[5], xr[6], xr[7]);
-                    } else {
-                        uint32_t pk[4];
-    #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            pk[i] = (__float_as_uint(xr[2 * i]) >> 16) | (__float_as_uint(xr[2 * i + 1]) & 0xFFFF0000u);
-                        *reinterpret_cast<uint4 *>(smem + L.xs + (size_t(v) * nsub_max + sl) * kXsB16 + oct * 16) =
-                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    }
-                    if (e8 == 0) {
-                        const int c = int(e) - 105;  // f1 * f2 = 2^c
-                        const int c1 = c < 127 ? c : 127;
-                        const float4 meta = make_float4(sx, __uint_as_float(uint32_t(c1 + 127) << 23),
-                                                        __uint_as_float(uint32_t(c - c1 + 127) << 23), 0.0f);
-                        if constexpr (V == 1)
-                            *reinterpret_cast<float4 *>(smem + L.xs + size_t(sl) * kXsF32 * 4 + 256) = meta;
-                        else
-                            *reinterpret_cast<float4 *>(smem + L.xs + (size_t(v) * nsub_max + sl) * kXsB16 + 128) = meta;
-                    }
-                }
-            }
-        }
-        // consumer warps only
-        asm volatile("bar.sync 1, %0;" ::"r"(C * 32) : "memory");
-
         // --------------------------------------------------------- consumers
-        uint32_t poff[T::NP];
+        grid_dependency_wait();  // x may be written by the preceding grid
+        stage_x<BITS, 1>(smem, L.xs, p.x, p.K, sub_lo, nsub, nsub_max, tid, C * 32);
+        asm volatile("bar.sync 1, %0;" ::"r"(C * 32) : "memory");  // consumer warps only
+
+        uint32_t poff[NP];
         piece_offsets<BITS>(lane, poff);
-        const uint32_t xv_bytes = uint32_t(nsub_max) * kXsB16;
         for (;;) {
             int u = 0;
             if (lane == 0) u = int(atomicAdd(s_next, 1u));
@@ -667,75 +765,43 @@ __device__ __forceinline__ void qmv_body(const CUtensorMap *map_s, const CUtenso
             const Unit g = unit_geo(u);
             const uint32_t base = ring + slot * L.slot_bytes;
             const int nbox = p.sb_mode_unit ? 1 : g.nr;
+            // Per-unit shared addresses of row r's scale / bias of group 0 of
+            // the row (rows past N alias row 0).
+            uint32_t sa[kRows], ba[kRows];
+            {
+                const int g0 = g.c0 * (kChunkElems / GS);
+#pragma unroll
+                for (int r = 0; r < kRows; ++r) {
+                    const int rr = r < g.nr ? r : 0;
+                    const int bx = p.sb_mode_unit ? 0 : rr;
+                    const int xst = int(((long long)(g.r0 + bx) * p.G + g0) & ~7ll);
+                    sa[r] = base + L.sb_off + bx * L.sbs + 2 * ((g.r0 + rr) * p.G - xst);
+                    ba[r] = sa[r] + nbox * L.sbs;
+                }
+            }
             for (int cc = g.c0; cc < g.c1; ++cc) {
                 const int t = cc * kChunkSubs + lane;        // subgroup index in the row
                 const bool active = t < p.S_row;
-                const int tl = active ? t : cc * kChunkSubs;  // a valid subgroup for idle lanes
-                const int ln = tl - cc * kChunkSubs;
-                // chunk offset inside a slot row
-                const uint32_t coff = uint32_t(p.full_rows ? cc * kChunkB : (cc - g.c0) * kChunkB);
-                uint32_t wrow[kRows][T::NP];
+                const int tl = active ? t : cc * kChunkSubs;  // a staged subgroup for idle lanes
+                // lanes past the row's end read subgroup 0 of the chunk (discarded)
+                const uint32_t coff = uint32_t((cc - g.c0) * kChunkB) - (active ? 0u : uint32_t(lane) * kSubB);
+                uint4 quads[kRows][NP];
 #pragma unroll
                 for (int r = 0; r < kRows; ++r)
 #pragma unroll
-                    for (int pc = 0; pc < T::NP; ++pc)
-                        wrow[r][pc] = base + r * p.pitch + coff + (active ? poff[pc] : poff[pc] - lane * kSubB + ln * kSubB);
-                // scale and bias of the lane's group in each row
-                const int gi = int((long long)tl * kSub / GS);
+                    for (int pc = 0; pc < NP; ++pc)
+                        quads[r][pc] = lds_v4_u32(base + uint32_t(r * p.pitch) + coff + poff[pc]);
+                const uint32_t gi2 = uint32_t(tl * (kSub / 32) / (GS / 32)) * 2;
                 float fs[kRows], fb[kRows];
 #pragma unroll
                 for (int r = 0; r < kRows; ++r) {
-                    const int bx = p.sb_mode_unit ? 0 : (r < g.nr ? r : 0);
-                    const int off = int((long long)(g.r0 + r) * p.G + gi - sb_coord(g, bx));
-                    const int offc = r < g.nr ? off : 0;
-                    fs[r] = bf16_bits_to_f32(lds_u16(base + L.sb_off + bx * L.sbs + offc * 2));
-                    fb[r] = bf16_bits_to_f32(lds_u16(base + L.sb_off + (nbox + bx) * L.sbs + offc * 2));
+                    fs[r] = bf16_bits_to_f32(lds_u16(sa[r] + gi2));
+                    fb[r] = bf16_bits_to_f32(lds_u16(ba[r] + gi2));
                 }
-                const int sl = tl - sub_lo;
-                if constexpr (V == 1) {
-                    const uint32_t xsub = xs + uint32_t(sl) * kXsF32 * 4;
-                    uint64_t acc[kRows];
-                    subgroup_dot_v1<BITS>(wrow, xsub, acc);
-                    const float4 meta = lds_f4(xsub + 256);
-                    float val[T::NRED];
-#pragma unroll
-                    for (int r = 0; r < kRows; ++r) {
-                        const float term = subgroup_term<false>(acc[r], fs[r], fb[r], meta.x, meta.y, meta.z);
-                        val[r] = active ? term : 0.0f;
-                    }
-                    const float tot = tree_reduce_scatter<T::NRED>(val, lane);
-                    const int r = lane >> 3;
-                    if ((lane & 7) == 0 && r < g.nr)
-                        cvs[(g.r0 - row_t0 + r) * cpc_here + (cc - c_lo)] = tot;
-                } else {
-#pragma unroll
-                    for (int ps = 0; ps < T::PASSES; ++ps) {
-                        const int v0 = ps * T::VP;
-                        const uint32_t xsub = xs + (uint32_t(v0) * nsub_max + sl) * kXsB16;
-                        uint64_t acc[kRows][T::VP];
-                        subgroup_dot_vp<BITS, T::VP>(wrow, xsub, xv_bytes, acc);
-                        float val[T::NRED];
-#pragma unroll
-                        for (int i = 0; i < T::NRED; ++i) val[i] = 0.0f;
-#pragma unroll
-                        for (int v = 0; v < T::VP; ++v) {
-                            if (v0 + v >= V) break;
-                            const float4 meta = lds_f4(xsub + v * xv_bytes + 128);
-#pragma unroll
-                            for (int r = 0; r < kRows; ++r) {
-                                const float term = subgroup_term<true>(acc[r][v], fs[r], fb[r], meta.x, meta.y, meta.z);
-                                val[r * T::VP + v] = active ? term : 0.0f;
-                            }
-                        }
-                        const float tot = tree_reduce_scatter<T::NRED>(val, lane);
-                        // lane holds value index lane >> (5 - log2 NRED)
-                        constexpr int SH = T::NRED == 4 ? 3 : T::NRED == 8 ? 2 : T::NRED == 16 ? 1 : 0;
-                        const int idx = lane >> SH;
-                        const int r = idx / T::VP, v = idx - r * T::VP;
-                        if ((lane & ((1 << SH) - 1)) == 0 && idx < T::NVAL && v0 + v < V && r < g.nr)
-                            cvs[((g.r0 - row_t0 + r) * cpc_here + (cc - c_lo)) * V + v0 + v] = tot;
-                    }
-                }
+                const float tot =
+                    chunk_v1<BITS>(quads, xs + uint32_t(tl - sub_lo) * kXsF32 * 4, fs, fb, active, lane);
+                const int r = lane >> 3;
+                if ((lane & 7) == 0 && r < g.nr) cvs[(g.r0 - row_t0 + r) * cpc_here + (cc - c_lo)] = tot;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * slot);
@@ -753,77 +819,174 @@ __device__ __forceinline__ void qmv_body(const CUtensorMap *map_s, const CUtenso
         __syncthreads();
         return;
     }
-
-    auto store_y = [&](int v, int n, float val) {
-        if (p.f32_out)
-            static_cast<float *>(p.y)[size_t(v) * p.N + n] = val;
-        else
-            static_cast<__nv_bfloat16 *>(p.y)[size_t(v) * p.N + n] = __float2bfloat16_rn(val);
-    };
-    const int nrows = (rb_hi - rb_lo) * kRows;
-
-    // Step 4: fold the chunk values left to right.
-    if (p.cpc >= p.ks) {
-        for (int idx = tid; idx < nrows * V; idx += nthreads) {
-            const int v = idx / nrows, r = idx - v * nrows;
-            const int n = row_t0 + r;
-            if (n >= p.N) continue;
-            float acc = cvs[(r * cpc_here) * V + v];
-            for (int c = 1; c < p.ks; ++c) acc = __fadd_rn(acc, cvs[(r * cpc_here + c) * V + v]);
-            store_y(v, n, acc);
-        }
-        return;
-    }
-
-    // A chunk range per CTA: publish its values; the CTA that completes the
-    // row range last folds all chunks left to right and zeroes what it read,
-    // so (with the self-resetting counter) the workspace is zero again.
-    for (int idx = tid; idx < nrows * V * cpc_here; idx += nthreads) {
-        const int cl = idx / (nrows * V), rem = idx - cl * nrows * V;
-        const int v = rem / nrows, r = rem - v * nrows;
-        const int n = row_t0 + r;
-        if (n < p.N) __stcg(p.partials + (size_t(c_lo + cl) * V + v) * p.N + n, cvs[(r * cpc_here + cl) * V + v]);
-    }
-    __threadfence();
-    __syncthreads();
-    const unsigned nranges = unsigned(gridDim.y);
-    if (tid == 0) s_ticket = atomicInc(p.counters + rb_lo, nranges - 1);
-    __syncthreads();
-    if (s_ticket != nranges - 1) return;
-    __threadfence();
-    for (int idx = tid; idx < nrows * V; idx += nthreads) {
-        const int v = idx / nrows, r = idx - v * nrows;
-        const int n = row_t0 + r;
-        if (n >= p.N) continue;
-        float *pp = p.partials + size_t(v) * p.N + n;
-        float acc = __ldcg(pp);
-        __stcg(pp, 0.0f);
-        for (int c = 1; c < p.ks; ++c) {
-            float *pc = pp + size_t(c) * V * p.N;
-            acc = __fadd_rn(acc, __ldcg(pc));
-            __stcg(pc, 0.0f);
-        }
-        store_y(v, n, acc);
-    }
+    fold_chunks<1>(cvs, (rb_hi - rb_lo) * kRows, row_t0, c_lo, cpc_here, rb_lo, tid, nthreads, p.N, p.ks, p.cpc,
+                   p.partials, p.counters, p.y, p.f32_out);
 }
 
-// Launch bounds: V = 1 runs 16 consumer warps + 4 producers; the streamed
-// kernel 10 + 2 (its registers go to the V-vector accumulators).
-constexpr int kThreadsV1 = 20 * 32;
+// ------------------------------------------------ V vectors: direct loads --
+
+template <int BITS, int GS, int V>
+__device__ __forceinline__ void qmv_direct_body(const Params &p)
+{
+    using T = Traits<BITS, V>;
+    constexpr int kSubB = sub_bytes(BITS);
+
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nthreads = blockDim.x;
+
+    const int c_lo = blockIdx.y * p.cpc;
+    const int c_hi = c_lo + p.cpc < p.ks ? c_lo + p.cpc : p.ks;
+    const int sub_lo = c_lo * kChunkSubs;
+    const int sub_hi = c_hi * kChunkSubs < p.S_row ? c_hi * kChunkSubs : p.S_row;
+    const int nsub = sub_hi - sub_lo;
+    const int rb_lo = int((long long)blockIdx.x * p.NB / p.grid_rows);
+    const int rb_hi = int((long long)(blockIdx.x + 1) * p.NB / p.grid_rows);
+    const int row_t0 = rb_lo * kRows;
+    const int cpc_here = c_hi - c_lo;
+    const int nunits = (rb_hi - rb_lo) * cpc_here;  // (row block, chunk) pairs
+
+    const int nsub_max = p.cpc * kChunkSubs < p.S_row ? p.cpc * kChunkSubs : p.S_row;
+    const SmemLayout L = smem_layout(BITS, V, nthreads >> 5, nsub_max, p.max_rb, p.cpc);
+    const uint32_t xs = smem_u32(smem + L.xs);
+    float *cvs = reinterpret_cast<float *>(smem + L.cv);
+    unsigned *s_next = reinterpret_cast<unsigned *>(smem + L.misc);
+    if (tid == 0) *s_next = 0;
+    __syncthreads();
+
+    uint32_t poff[T::NP];
+    piece_offsets<BITS>(lane, poff);
+    // The next unit for this warp (units are taken in increasing order).
+    auto grab = [&]() {
+        int u = 0;
+        if (lane == 0) u = int(atomicAdd(s_next, 1u));
+        return __shfl_sync(0xffffffffu, u, 0);
+    };
+    struct Unit {
+        int r0, nr, cc, t, tc;  // rows [r0, r0 + nr), chunk cc, the lane's subgroup (tc: clamped into the row)
+    };
+    auto unit_geo = [&](int u) {
+        Unit g;
+        const int rbl = u / cpc_here;
+        g.r0 = (rb_lo + rbl) * kRows;
+        g.nr = p.N - g.r0 < kRows ? p.N - g.r0 : kRows;
+        g.cc = c_lo + (u - rbl * cpc_here);
+        g.t = g.cc * kChunkSubs + lane;
+        g.tc = g.t < p.S_row ? g.t : p.S_row - 1;
+        return g;
+    };
+    // Unit u's weight bytes of this lane (4 rows x its subgroup, pieces in
+    // processing order), and the scale and bias of its group in each row.
+    // Rows past N and subgroups past the row's end re-read valid bytes
+    // (their results are discarded).
+    auto load_unit = [&](int u, uint4 (&wq)[kRows][T::NP], uint32_t (&sv)[kRows], uint32_t (&bv)[kRows]) {
+        const Unit g = unit_geo(u);
+        const int gi = g.tc * (kSub / 32) / (GS / 32);
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+            const int row = g.r0 + (r < g.nr ? r : 0);
+            const uint8_t *src = p.w + size_t(row) * p.row_bytes + size_t(g.tc) * kSubB;
+#pragma unroll
+            for (int pc = 0; pc < T::NP; ++pc)
+                wq[r][pc] = __ldg(reinterpret_cast<const uint4 *>(src + (BITS == 4 ? (poff[pc] & 31u) : 0u)));
+            const size_t e = size_t(row) * p.G + gi;
+            sv[r] = __ldg(p.scales + e);
+            bv[r] = __ldg(p.biases + e);
+        }
+    };
+
+    // The first unit's loads first: they do not depend on the preceding grid,
+    // so their latency overlaps its tail and the staging of x below.
+    int u0 = grab();
+    uint4 w_cur[kRows][T::NP];
+    uint32_t s_cur[kRows] = {0, 0, 0, 0}, b_cur[kRows] = {0, 0, 0, 0};
+    if (u0 < nunits) load_unit(u0, w_cur, s_cur, b_cur);
+    grid_launch_dependents();
+    grid_dependency_wait();  // x may be written by the preceding grid
+    stage_x<BITS, V>(smem, L.xs, p.x, p.K, sub_lo, nsub, nsub_max, tid, nthreads);
+    __syncthreads();
+
+    const uint32_t xv_bytes = uint32_t(nsub_max) * kXsB16;
+    const uint32_t wcell = smem_u32(smem + L.wbuf) + uint32_t(warp) * kRows * T::NP * 512u + uint32_t(lane) * 16u;
+    while (u0 < nunits) {
+        const Unit g = unit_geo(u0);
+        const bool active = g.t < p.S_row;
+        const int sl = (active ? g.t : g.cc * kChunkSubs) - sub_lo;  // a staged subgroup for idle lanes
+        float fs[kRows], fb[kRows];
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+            fs[r] = bf16_bits_to_f32(s_cur[r]);
+            fb[r] = bf16_bits_to_f32(b_cur[r]);
+        }
+        // two passes: park the weight bytes in this lane's cells of the
+        // warp's buffer (only this lane reads them back)
+        if constexpr (T::PASSES > 1) {
+#pragma unroll
+            for (int r = 0; r < kRows; ++r)
+#pragma unroll
+                for (int pc = 0; pc < T::NP; ++pc) sts_v4_u32(wcell + uint32_t(r * T::NP + pc) * 512u, w_cur[r][pc]);
+        }
+#pragma unroll
+        for (int ps = 0; ps < T::PASSES; ++ps) {
+            const int v0 = ps * T::VP;
+            const uint32_t xsub = xs + (uint32_t(v0) * nsub_max + sl) * kXsB16;
+            uint64_t acc[kRows][T::VP];
+            if constexpr (T::PASSES > 1)
+                subgroup_dot_vp_smem<BITS, T::VP>(wcell, xsub, xv_bytes, acc);
+            else
+                subgroup_dot_vp<BITS, T::VP>(w_cur, xsub, xv_bytes, acc);
+            float val[T::NRED];
+#pragma unroll
+            for (int i = 0; i < T::NRED; ++i) val[i] = 0.0f;
+#pragma unroll
+            for (int v = 0; v < T::VP; ++v) {
+                if (v0 + v >= V) break;
+                const float4 meta = lds_f4(xsub + v * xv_bytes + 128);
+#pragma unroll
+                for (int r = 0; r < kRows; ++r) {
+                    const float term = subgroup_term<true>(acc[r][v], fs[r], fb[r], meta.x, meta.y, meta.z);
+                    val[r * T::VP + v] = active ? term : 0.0f;
+                }
+            }
+            const float tot = tree_reduce_scatter<T::NRED>(val, lane);
+            // lane holds value index lane >> (5 - log2 NRED)
+            constexpr int SH = T::NRED == 4 ? 3 : T::NRED == 8 ? 2 : T::NRED == 16 ? 1 : 0;
+            const int idx = lane >> SH;
+            const int r = idx / T::VP, v = idx - r * T::VP;
+            if ((lane & ((1 << SH) - 1)) == 0 && idx < T::NVAL && v0 + v < V && r < g.nr)
+                cvs[((g.r0 - row_t0 + r) * cpc_here + (g.cc - c_lo)) * V + v0 + v] = tot;
+        }
+        // the next unit: its loads are issued only now (the other warps'
+        // arithmetic covers their latency)
+        u0 = grab();
+        if (u0 < nunits) load_unit(u0, w_cur, s_cur, b_cur);
+    }
+    __syncthreads();
+    fold_chunks<V>(cvs, (rb_hi - rb_lo) * kRows, row_t0, c_lo, cpc_here, rb_lo, tid, nthreads, p.N, p.ks, p.cpc,
+                   p.partials, p.counters, p.y, p.f32_out);
+}
+
+// Launch bounds: the one-vector kernel runs 16 consumer warps and 4 producer
+// warps; the streamed kernel 12 warps (its registers go to the V-vector
+// accumulators).
+constexpr int kConsumersV1 = 16;
+constexpr int kProducersV1 = 4;
+constexpr int kThreadsV1 = (kConsumersV1 + kProducersV1) * 32;
 constexpr int kThreadsVN = 12 * 32;
 
 template <int BITS, int GS>
 __global__ void __launch_bounds__(kThreadsV1, 1)
-    qmv_m1(const __grid_constant__ CUtensorMap map_s, const __grid_constant__ CUtensorMap map_b, const Params p)
+    qmv_m1(const __grid_constant__ CUtensorMap map_s, const __grid_constant__ CUtensorMap map_b, const RingParams p)
 {
-    qmv_body<BITS, GS, 1>(&map_s, &map_b, p);
+    qmv_ring_body<BITS, GS>(&map_s, &map_b, p);
 }
 
 template <int BITS, int GS, int V>
-__global__ void __launch_bounds__(kThreadsVN, 1)
-    qmv_streamed(const __grid_constant__ CUtensorMap map_s, const __grid_constant__ CUtensorMap map_b, const Params p)
+__global__ void __launch_bounds__(kThreadsVN, 1) qmv_streamed(const Params p)
 {
-    qmv_body<BITS, GS, V>(&map_s, &map_b, p);
+    qmv_direct_body<BITS, GS, V>(p);
 }
 
 }  // namespace qmv

@@ -8,9 +8,11 @@
 
 namespace qmv {
 
-template <typename Kern>
-cudaError_t launch_one(Kern kern, int (&configured)[64], const CUtensorMap &map_s, const CUtensorMap &map_b,
-                       const Params &p, const Launch &l, cudaStream_t stream)
+static_assert(kConsumersV1 == kRingConsumers && kProducersV1 == kRingProducers, "launch bounds");
+static_assert(kThreadsVN == kStreamedWarps * 32, "launch bounds");
+
+template <typename Kern, typename... Args>
+cudaError_t launch_one(Kern kern, int (&configured)[64], const Launch &l, cudaStream_t stream, Args... args)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -33,30 +35,33 @@ cudaError_t launch_one(Kern kern, int (&configured)[64], const CUtensorMap &map_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = l.pdl ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, kern, map_s, map_b, p);
+    e = cudaLaunchKernelEx(&cfg, kern, args...);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-template <int BITS, int GS, int V>
-cudaError_t launch_v(const CUtensorMap &map_s, const CUtensorMap &map_b, const Params &p, const Launch &l,
-                     cudaStream_t stream)
+template <int BITS, int GS>
+cudaError_t launch_m1(const CUtensorMap &map_s, const CUtensorMap &map_b, const RingParams &p, const Launch &l,
+                      cudaStream_t stream)
 {
     static int configured[64] = {0};
-    if constexpr (V == 1)
-        return launch_one(qmv_m1<BITS, GS>, configured, map_s, map_b, p, l, stream);
-    else
-        return launch_one(qmv_streamed<BITS, GS, V>, configured, map_s, map_b, p, l, stream);
+    return launch_one(qmv_m1<BITS, GS>, configured, l, stream, map_s, map_b, p);
+}
+
+template <int BITS, int GS, int V>
+cudaError_t launch_v(const Params &p, const Launch &l, cudaStream_t stream)
+{
+    static int configured[64] = {0};
+    return launch_one(qmv_streamed<BITS, GS, V>, configured, l, stream, p);
 }
 
 template <int BITS, int GS>
-cudaError_t launch_bits_gs(int V, const CUtensorMap &map_s, const CUtensorMap &map_b, const Params &p,
-                           const Launch &l, cudaStream_t stream)
+cudaError_t launch_streamed(int V, const Params &p, const Launch &l, cudaStream_t stream)
 {
     switch (V) {
 #define QMV_CASE(v) \
-    case v: return launch_v<BITS, GS, v>(map_s, map_b, p, l, stream);
-        QMV_CASE(1) QMV_CASE(2) QMV_CASE(3) QMV_CASE(4) QMV_CASE(5) QMV_CASE(6) QMV_CASE(7) QMV_CASE(8)
+    case v: return launch_v<BITS, GS, v>(p, l, stream);
+        QMV_CASE(2) QMV_CASE(3) QMV_CASE(4) QMV_CASE(5) QMV_CASE(6) QMV_CASE(7) QMV_CASE(8)
         QMV_CASE(9) QMV_CASE(10) QMV_CASE(11) QMV_CASE(12) QMV_CASE(13) QMV_CASE(14) QMV_CASE(15) QMV_CASE(16)
 #undef QMV_CASE
         default: return cudaErrorInvalidValue;

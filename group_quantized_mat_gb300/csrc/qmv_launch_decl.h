@@ -8,10 +8,11 @@
 
 namespace qmv {
 
-// Warps per CTA of the kernel for V vectors (its launch bounds): consumer
-// warps, then producer warps.
-inline int consumer_warps(int V) { return V == 1 ? 16 : 10; }
-inline int producer_warps(int V) { return V == 1 ? 4 : 2; }
+// Warps per CTA of the streamed kernel (its launch bounds), and the one-vector
+// kernel's consumer and producer warps.
+constexpr int kStreamedWarps = 12;
+constexpr int kRingConsumers = 16;
+constexpr int kRingProducers = 4;
 
 struct Launch {
     dim3 grid;
@@ -20,9 +21,10 @@ struct Launch {
     bool pdl;  // launch with a programmatic dependency on the preceding grid
 };
 
-#define QMV_DECLARE_LAUNCH(name) \
-    cudaError_t name(int V, const CUtensorMap &map_s, const CUtensorMap &map_b, const Params &p, const Launch &l, \
-                     cudaStream_t stream);
+#define QMV_DECLARE_LAUNCH(name)                                                                                  \
+    cudaError_t name##_m1(const CUtensorMap &map_s, const CUtensorMap &map_b, const RingParams &p, const Launch &l, \
+                          cudaStream_t stream);                                                                   \
+    cudaError_t name##_streamed(int V, const Params &p, const Launch &l, cudaStream_t stream);
 QMV_DECLARE_LAUNCH(launch_b4g64)
 QMV_DECLARE_LAUNCH(launch_b4g128)
 QMV_DECLARE_LAUNCH(launch_b2g64)

@@ -18,27 +18,24 @@ constexpr int kRows = 4;            // rows per work unit; every lane of the war
 constexpr int kMaxM = 16;
 constexpr int kXsF32 = 68;          // floats per staged subgroup, fp32 layout: 64 x' + (sx, f1, f2, 0)
 constexpr int kXsB16 = 144;         // bytes per staged subgroup, bf16 layout: 128 B x' + (sx, f1, f2, 0)
-constexpr int kBoxAlign = 128;      // shared-memory alignment of a tensor-map box
 
 __host__ __device__ constexpr int sub_bytes(int bits) { return kSub * bits / 8; }
 __host__ __device__ constexpr int chunk_bytes(int bits) { return kChunkElems * bits / 8; }
 __host__ __device__ inline int subs_per_row(int K) { return K / kSub; }
 // Number of K-chunks of a row (the last one may hold fewer than 32 subgroups).
 __host__ __device__ inline int chunk_count(int K) { return (subs_per_row(K) + kChunkSubs - 1) / kChunkSubs; }
-__host__ __device__ inline int round_down8(long long v) { return int(v & ~7ll); }
 
-// Kernel arguments other than the tensor maps.
+// Arguments common to both kernels.
 //
 // CTA (i, j) owns the row blocks [i*NB/grid_rows, (i+1)*NB/grid_rows) (4 rows
-// each) and the chunks [j*cpc, min((j+1)*cpc, ks)). Its work units are
-// (row block, piece) pairs, a piece being uc consecutive chunks of the CTA's
-// range; unit u = row block u / upr, piece u % upr. One producer warp streams
-// the units in order through a ring of `slots` shared-memory slots; the
-// consumer warps take units dynamically. Chunk values meet in shared memory;
-// with cpc = ks the CTA folds them into y, otherwise they go through the
-// workspace and the CTA that completes a row range last folds all ks of them.
+// each) and the chunks [j*cpc, min((j+1)*cpc, ks)). Chunk values meet in
+// shared memory; with cpc = ks the CTA folds them into y, otherwise they go
+// through the workspace and the CTA that completes a row range last folds all
+// ks of them.
 struct Params {
     const uint8_t *w;         // packed weights [N, row_bytes]
+    const uint16_t *scales;   // bf16 bits [N, G]
+    const uint16_t *biases;   // bf16 bits [N, G]
     const uint16_t *x;        // bf16 bits [V, K]
     void *y;                  // bf16 bits or float [V, N]
     float *partials;          // [ks, V, N] when cpc < ks
@@ -51,39 +48,66 @@ struct Params {
     int NB;                   // row blocks of the matrix
     int grid_rows;            // CTAs along the rows
     int cpc;                  // chunks per CTA
+    int max_rb;               // row blocks of the largest CTA share
+    int f32_out;
+};
+
+// The one-vector kernel's ring: units are (row block, piece) pairs, a piece
+// being uc consecutive chunks of the CTA's range; producer warps stream them
+// through `slots` shared-memory slots (weights, then the scale and bias
+// boxes) and the consumer warps take them in order from a shared counter.
+struct RingParams : Params {
     int uc;                   // chunks per unit
     int full_rows;            // 1: a unit is whole rows, loaded as one contiguous copy
     int pitch;                // bytes per unit row in a slot
     int sb_mode_unit;         // 1: one scale box and one bias box per unit; 0: one of each per row
     int sbox;                 // elements per scale / bias box (a multiple of 8)
-    int slots;                // ring slots
-    int consumers;            // consumer warps; the producer is warp `consumers`
-    int max_rb;               // row blocks of the largest CTA share
-    int f32_out;
-};
-
-// Shared memory of one CTA, as byte offsets from a 128-aligned base.
-struct SmemLayout {
-    int slot_bytes, sb_off, sbs;  // slot size, offset of the scale/bias boxes in a slot, bytes per box
-    int ring, xs, cv, bar, misc, total;
+    int slots;                // ring slots (a multiple of the producer warps)
+    int consumers;            // consumer warps; warps consumers.. are producers
 };
 
 __host__ __device__ inline int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
-// nsub: subgroups of x the CTA stages (per vector); V: vectors.
-__host__ __device__ inline SmemLayout smem_layout(int bits, int V, int pitch, int sb_mode_unit, int sbox, int slots,
-                                                  int nsub, int max_rb, int cpc)
+// Vectors per pass of the streamed kernel (two passes above eight).
+__host__ __device__ constexpr int vectors_per_pass(int V) { return V <= 8 ? V : (V + 1) / 2; }
+
+// Shared memory of the streamed kernel, as byte offsets from a 128-aligned
+// base: staged x, chunk values, and (two passes) each warp's unit of weights
+// (4 rows x 32 lanes x one subgroup).
+struct SmemLayout {
+    int xs, cv, wbuf, misc, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int bits, int V, int warps, int nsub, int max_rb, int cpc)
 {
-    (void)bits;
     SmemLayout L;
+    L.xs = 0;
+    L.cv = align_up(V * nsub * kXsB16, 16);
+    L.wbuf = align_up(L.cv + max_rb * kRows * cpc * V * 4, 16);
+    L.misc = L.wbuf + (vectors_per_pass(V) < V ? warps * kRows * 32 * sub_bytes(bits) : 0);
+    L.total = L.misc + 16 + 128;  // next-unit counter; slack for aligning the dynamic base
+    return L;
+}
+
+// Shared memory of the one-vector kernel, as byte offsets from a 128-aligned
+// base: the ring, staged x, chunk values, the slot barriers and counters.
+constexpr int kBoxAlign = 128;  // shared-memory alignment of a tensor-map box
+struct RingLayout {
+    int slot_bytes, sb_off, sbs;  // slot size, offset of the scale/bias boxes in a slot, bytes per box
+    int ring, xs, cv, bar, misc, total;
+};
+
+__host__ __device__ inline RingLayout ring_layout(int pitch, int sb_mode_unit, int sbox, int slots, int nsub, int max_rb,
+                                                  int cpc)
+{
+    RingLayout L;
     L.sbs = align_up(sbox * 2, kBoxAlign);
     L.sb_off = align_up(kRows * pitch, kBoxAlign);
     L.slot_bytes = L.sb_off + (sb_mode_unit ? 2 : 2 * kRows) * L.sbs;
     L.ring = 0;
     L.xs = slots * L.slot_bytes;
-    const int xs_bytes = V == 1 ? nsub * kXsF32 * 4 : V * nsub * kXsB16;
-    L.cv = align_up(L.xs + xs_bytes, 16);
-    L.bar = align_up(L.cv + max_rb * kRows * cpc * V * 4, 16);
+    L.cv = align_up(L.xs + nsub * kXsF32 * 4, 16);
+    L.bar = align_up(L.cv + max_rb * kRows * cpc * 4, 16);
     L.misc = L.bar + 2 * slots * 8;
     L.total = L.misc + 32 + kBoxAlign;  // next-unit counter, abort flag, issued counts; alignment slack
     return L;

@@ -198,11 +198,11 @@ QMV_API qmv_status qmv_workspace_init(void *workspace, size_t bytes, qmv_stream_
 
 /* ------------------------------------------------------------ diagnostics */
 
-/* Device-side error word of the current device: kernels set bit 0 when a
- * bounded wait for a weight tile ran out, bit 1 when a launch shape violated
- * the shared-memory ring protocol (neither happens with the library's own
- * launch plans; the output of that launch is then invalid). Synchronizes the
- * device, stores the word in *word and clears it.
+/* Device-side error word of the current device: the one-vector kernel sets
+ * bit 0 when a bounded wait for a weight tile ran out and bit 1 when a launch
+ * shape breaks its shared-memory ring protocol (neither happens with the
+ * library's own launch plans; the output of that launch is then invalid).
+ * Synchronizes the device, stores the word in *word and clears it.
  * Errors: QMV_ERR_NULL, QMV_ERR_CUDA. */
 QMV_API qmv_status qmv_device_error(unsigned *word);
 

@@ -100,17 +100,17 @@ def test_split_plan(lib):
     assert g.qmv_split_count(1, 1000, 4, 64) == 0
     assert g.qmv_workspace_size(1, 256, 1024, 4, 64) == 0
     # one CTA covers all chunks of its rows (no workspace) while the staged x
-    # of all of K fits: M = 1 on both projections, M = 13 on K = 3840
+    # of all of K fits: M = 1 on both projections, M up to 16 on K = 3840
     assert g.qmv_workspace_size(1, 15360, 3840, 4, 64) == 0
     assert g.qmv_workspace_size(1, 3840, 15360, 4, 64) == 0
     assert g.qmv_workspace_size(13, 15360, 3840, 4, 64) == 0
-    # otherwise one chunk per CTA; chunk values meet in the workspace after a
-    # 256-byte-aligned block of one counter per 4-row block
-    NB = 15360 // 4
-    w16 = g.qmv_workspace_size(16, 15360, 3840, 4, 64)
-    assert w16 == (NB * 4 + 255) // 256 * 256 + 2 * 16 * 15360 * 4
+    assert g.qmv_workspace_size(16, 15360, 3840, 4, 64) == 0
+    # otherwise a range of chunks per CTA; chunk values meet in the workspace
+    # after a 256-byte-aligned block of one counter per 4-row block
     w13 = g.qmv_workspace_size(13, 3840, 15360, 4, 64)
     assert w13 == (960 * 4 + 255) // 256 * 256 + 8 * 13 * 3840 * 4
+    w16 = g.qmv_workspace_size(16, 3840, 15360, 4, 64)
+    assert w16 - w13 == 8 * 3 * 3840 * 4
     assert g.qmv_workspace_size(17, 15360, 3840, 4, 64) == 0
     # sizes whose scale index would pass 2^31 are refused
     assert g.qmv_split_count(1 << 30, 1 << 13, 4, 64) == 0
