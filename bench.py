@@ -43,9 +43,10 @@ WORKLOAD = "proj_15360x3840_4b_g64"
 KERNEL_SOURCES = ["qmv_kernel.cuh", "qmv_plan.h"]
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes per launch of qmv_m1 read from one ncu capture, keyed by a hash of
-# the kernel sources it was taken on (None until a capture exists).
-NCU_TRAFFIC = {}
+# DRAM bytes per launch of qmv_m1 (dram__bytes_read.sum + dram__bytes_write.sum)
+# from one ncu capture of the bench workload, keyed by a hash of the kernel
+# sources it was taken on; a changed kernel reports null until recaptured.
+NCU_TRAFFIC = {"e615fa567117d023": 33241600}
 
 
 def kernel_hash() -> str:
@@ -58,6 +59,23 @@ def kernel_hash() -> str:
 
 def algorithmic_bytes(N, K, M, bits, gs):
     return N * K * bits // 8 + 4 * N * (K // gs) + 2 * M * (K + N)
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of every rank's `value` (timed-region milliseconds): the
+    job's time. One rank: the value itself."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_call: int, calls_per_rank: int, world: int, job_ms: float) -> float:
+    """Whole-job throughput: the bytes all ranks processed over the job's time."""
+    return world * calls_per_rank * bytes_per_call / (job_ms * 1e-3) / 1e9
 
 
 def measured_peaks():
@@ -199,11 +217,7 @@ def run_gpu(args, rank, world, local_rank):
             torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
-        ms = start.elapsed_time(end)
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms = float(t.item())
+        ms = max_over_ranks(start.elapsed_time(end), world, dev)
         return ms, clk.summary()
 
     def measure_e2e(M, steps):
@@ -346,7 +360,8 @@ def main():
     if world > 1:
         import torch
         import torch.distributed as dist
-        torch.cuda.set_device(local_rank)
+        if args.impl == "ours":
+            torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
 
     if args.impl == "reference":
@@ -363,8 +378,8 @@ def main():
         b13 = algorithmic_bytes(N, K, 13, bits, gs)
         us1 = r["ms1"] * 1e3 / args.steps
         us13 = r["ms13"] * 1e3 / args.steps
-        gbs1 = b1 / (us1 * 1e-6) / 1e9
-        gbs13 = b13 / (us13 * 1e-6) / 1e9
+        gbs1 = whole_job_gbs(b1, args.steps, 1, r["ms1"])  # per GPU
+        gbs13 = whole_job_gbs(b13, args.steps, 1, r["ms13"])
         peak, peak_kind = measured_peaks()
         cpu_t, cpu_threads, cpu_rows, cpu_runs = oracle_timing(N, K, 1, bits, gs, seconds=args.cpu_seconds)
         cpu_gbs = b1 / cpu_t / 1e9
@@ -376,7 +391,7 @@ def main():
         flops13 = 2.0 * N * K * 13
         line = {
             "metric": METRIC,
-            "value": round(world * gbs1, 2),
+            "value": round(whole_job_gbs(b1, args.steps, world, r["ms1"]), 2),
             "unit": "GB/s",
             "n_gpus": world,
             "steps": args.steps,
