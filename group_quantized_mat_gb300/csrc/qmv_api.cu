@@ -147,8 +147,8 @@ Problem plan_ring(int N, int K, int bits, int gs, int sms)
 {
     Problem pr{};
     common_shape(pr, 1, N, K, bits, gs);
-    const int per_chunk = qmv::kChunkSubs * qmv::kXsF32 * 4;
-    pr.cpc = pr.S_row * qmv::kXsF32 * 4 <= kXsBudgetV1 ? pr.ks : kXsBudgetV1 / per_chunk;
+    const int per_chunk = qmv::kChunkSubs * qmv::kXsB16;
+    pr.cpc = pr.S_row * qmv::kXsB16 <= kXsBudgetV1 ? pr.ks : kXsBudgetV1 / per_chunk;
     pr.consumers = qmv::kRingConsumers;
 #if defined(QMV_TUNING)
     if (g_tune.cpc > 0 && g_tune.cpc <= pr.ks) pr.cpc = g_tune.cpc;
@@ -156,7 +156,11 @@ Problem plan_ring(int N, int K, int bits, int gs, int sms)
 #endif
     grid_shape(pr, sms, 1);
     const int cb = qmv::chunk_bytes(bits);
-    if (pr.cpc == pr.ks && qmv::kRows * pr.row_bytes <= kUnitMax) {
+    bool whole = pr.cpc == pr.ks && qmv::kRows * pr.row_bytes <= kUnitMax;
+#if defined(QMV_TUNING)
+    if (g_tune.uc > 0) whole = false;
+#endif
+    if (whole) {
         pr.full_rows = 1;
         pr.uc = pr.ks;
         pr.pitch = pr.row_bytes;

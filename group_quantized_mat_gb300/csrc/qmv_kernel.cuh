@@ -11,15 +11,14 @@
 // Fixed fp32 order of output (m, n), the same for every V:
 //  1. subgroup t (64 consecutive elements of row n, inside one quantization
 //     group g): with E the largest exponent field among its 64 bf16 x values
-//     (at least 1), each x_i is staged as x'_i = x_i * 2^(254 - bits*k_i - E)
-//     (k_i = position of element i inside its 16-bit half word), exactly a
-//     bf16 value, and each field q_i is read as the fp32 whose bit pattern is
-//     q_i << (bits*k_i) -- the subnormal q_i * 2^(bits*k_i - 149) -- so every
-//     product equals q_i * x_i * 2^(105 - E) exactly (for all x_i down to
-//     2^-120 times the subgroup's largest). Two running sums a_e, a_o over the
-//     even and odd elements in processing order from +0, one packed
-//     fma.rn.f32x2 per element pair; d = ((a_e + a_o) * f1) * f2 with
-//     f1 * f2 = 2^(E - 105);
+//     (at least 1), every product is q_i * x_i * 2^(105 - E), formed exactly
+//     inside an fma. Two running sums a_e, a_o over the even and odd elements
+//     in processing order from +0, one fma per element;
+//     d = ((a_e + a_o) * f1) * f2 with f1 * f2 = 2^(E - 105).
+//     The kernels reach the same product two ways (below, "field readings");
+//     an x_i whose exponent field is more than 231 below E is staged as a
+//     zero of its sign in both (its product would lie below 2^-247, far under
+//     the fp32 grid), so that both stagings are exact for every other x_i;
 //  2. term = fma(s_g, d, b_g * sx), sx = sum of the subgroup's 64 x: eight
 //     sums of eight consecutive elements (each left to right) added left to
 //     right;
@@ -28,6 +27,18 @@
 //     then (l, l^8), (l, l^4), (l, l^2), (l, l^1);
 //  4. y = ((c_0 + c_1) + c_2) + ... over the chunks of the row;
 //  5. one rounding to bf16, nearest even.
+// Field readings (both give the products of step 1 bit for bit):
+//  * qmv_streamed: x'_i = x_i * 2^(254 - bits*k_i - E), k_i = position of
+//    element i inside its 16-bit half word, staged as bf16; field q_i is the
+//    fp32 whose bit pattern is q_i << (bits*k_i), the subnormal
+//    q_i * 2^(bits*k_i - 149); one fma.rn.f32x2 per element pair.
+//  * qmv_m1: x''_i = x_i * 2^(238 - bits*j_i - E), j_i = position of the
+//    field inside its byte, staged as bf16; field q_i is the bf16 half whose
+//    bit pattern is q_i << (bits*j_i), i.e. q_i * 2^(bits*j_i - 133) (the low
+//    byte of a bf16 read as an integer n is n * 2^-133 exactly). One mask
+//    isolates two fields (one per 16-bit half), and fma.rn.f32.bf16 (exact
+//    product, fp32 sum, one rounding) takes each half: half the integer work
+//    of the fp32 reading, which is what bounds a one-vector pass.
 // Processing order inside a 4-bit subgroup: its two 16-byte halves, the half
 // selected by bit 2 of the subgroup index first (that keeps the eight lanes of
 // a shared-memory phase on distinct banks when a warp reads 32 subgroups of a
@@ -244,6 +255,27 @@ __device__ __forceinline__ uint32_t hi_half(uint32_t w)
     return h;
 }
 
+// a + (bf16 half WH of w) * (bf16 half XH of x): exact product, fp32 sum,
+// one rounding.
+template <int WH, int XH>
+__device__ __forceinline__ float fma_bf16(uint32_t w, uint32_t x, float a)
+{
+    float d;
+    if constexpr (WH == 0 && XH == 0)
+        asm("{.reg .b16 wl, wh, xl, xh;\n\tmov.b32 {wl, wh}, %1;\n\tmov.b32 {xl, xh}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, wl, xl, %3;}" : "=f"(d) : "r"(w), "r"(x), "f"(a));
+    else if constexpr (WH == 0)
+        asm("{.reg .b16 wl, wh, xl, xh;\n\tmov.b32 {wl, wh}, %1;\n\tmov.b32 {xl, xh}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, wl, xh, %3;}" : "=f"(d) : "r"(w), "r"(x), "f"(a));
+    else if constexpr (XH == 0)
+        asm("{.reg .b16 wl, wh, xl, xh;\n\tmov.b32 {wl, wh}, %1;\n\tmov.b32 {xl, xh}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, wh, xl, %3;}" : "=f"(d) : "r"(w), "r"(x), "f"(a));
+    else
+        asm("{.reg .b16 wl, wh, xl, xh;\n\tmov.b32 {wl, wh}, %1;\n\tmov.b32 {xl, xh}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, wh, xh, %3;}" : "=f"(d) : "r"(w), "r"(x), "f"(a));
+    return d;
+}
+
 // The four element pairs of an octet (8 consecutive elements in processing
 // order) as fp32 bit patterns q << (bits*k): one mask per element.
 //   4-bit: the octet is one word; pairs (0,1), (2,3) from its low half and
@@ -299,28 +331,70 @@ __device__ __forceinline__ void piece_offsets(int lane, uint32_t (&off)[BITS == 
     }
 }
 
-// Step 1 for V = 1: acc[r] = (a_e, a_o) of the lane's subgroup in rows 0..3.
+// Step 1 for V = 1 in the bf16 field reading: ae[r], ao[r] of the lane's
+// subgroup in rows 0..3.
 //   quads[r]  the subgroup's bytes in row r (16-byte pieces, processing order);
-//   xsub      shared address of the staged subgroup (64 fp32 x').
+//   xsub      shared address of the staged subgroup (64 bf16 x'', octets in
+//             processing order, 16 bytes each).
+// A 4-bit octet is one word w: fields (0,4), (1,5), (2,6), (3,7) sit in the
+// two halves of w & 0x000F000F, w & 0x00F000F0 and the same masks of w >> 8.
+// A 2-bit word holds octets 2p (low halves) and 2p + 1 (high halves): fields
+// k and k + 4 of both in the masks 3 << 2k of w and of w >> 8.
 template <int BITS>
 __device__ __forceinline__ void subgroup_dot_v1(const uint4 (&quads)[kRows][BITS == 4 ? 2 : 1], uint32_t xsub,
-                                                uint64_t (&acc)[kRows])
+                                                float (&ae)[kRows], float (&ao)[kRows])
 {
 #pragma unroll
-    for (int r = 0; r < kRows; ++r) acc[r] = 0ull;
+    for (int r = 0; r < kRows; ++r) ae[r] = ao[r] = 0.0f;
+    if constexpr (BITS == 4) {
 #pragma unroll
-    for (int o = 0; o < 8; ++o) {
-        uint64_t x01, x23, x45, x67;
-        lds_v2_u64(xsub + o * 32, x01, x23);
-        lds_v2_u64(xsub + o * 32 + 16, x45, x67);
+        for (int o = 0; o < 8; ++o) {
+            const uint4 X = lds_v4_u32(xsub + o * 16);
 #pragma unroll
-        for (int r = 0; r < kRows; ++r) {
-            uint64_t q[4];
-            subgroup_octet<BITS>(quads[r], o, q);
-            acc[r] = ffma2(q[0], x01, acc[r]);
-            acc[r] = ffma2(q[1], x23, acc[r]);
-            acc[r] = ffma2(q[2], x45, acc[r]);
-            acc[r] = ffma2(q[3], x67, acc[r]);
+            for (int r = 0; r < kRows; ++r) {
+                const uint32_t w = word_of(quads[r][o >> 2], o & 3), w8 = w >> 8;
+                const uint32_t m0 = w & 0x000F000Fu, m1 = w & 0x00F000F0u;
+                const uint32_t m2 = w8 & 0x000F000Fu, m3 = w8 & 0x00F000F0u;
+                ae[r] = fma_bf16<0, 0>(m0, X.x, ae[r]);
+                ao[r] = fma_bf16<0, 1>(m1, X.x, ao[r]);
+                ae[r] = fma_bf16<0, 0>(m2, X.y, ae[r]);
+                ao[r] = fma_bf16<0, 1>(m3, X.y, ao[r]);
+                ae[r] = fma_bf16<1, 0>(m0, X.z, ae[r]);
+                ao[r] = fma_bf16<1, 1>(m1, X.z, ao[r]);
+                ae[r] = fma_bf16<1, 0>(m2, X.w, ae[r]);
+                ao[r] = fma_bf16<1, 1>(m3, X.w, ao[r]);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int pw = 0; pw < 4; ++pw) {
+            const uint4 X0 = lds_v4_u32(xsub + pw * 32), X1 = lds_v4_u32(xsub + pw * 32 + 16);
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) {
+                const uint32_t w = word_of(quads[r][0], pw), w8 = w >> 8;
+                uint32_t m[8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    m[k] = w & (0x00030003u << (2 * k));
+                    m[k + 4] = w8 & (0x00030003u << (2 * k));
+                }
+                ae[r] = fma_bf16<0, 0>(m[0], X0.x, ae[r]);
+                ao[r] = fma_bf16<0, 1>(m[1], X0.x, ao[r]);
+                ae[r] = fma_bf16<0, 0>(m[2], X0.y, ae[r]);
+                ao[r] = fma_bf16<0, 1>(m[3], X0.y, ao[r]);
+                ae[r] = fma_bf16<0, 0>(m[4], X0.z, ae[r]);
+                ao[r] = fma_bf16<0, 1>(m[5], X0.z, ao[r]);
+                ae[r] = fma_bf16<0, 0>(m[6], X0.w, ae[r]);
+                ao[r] = fma_bf16<0, 1>(m[7], X0.w, ao[r]);
+                ae[r] = fma_bf16<1, 0>(m[0], X1.x, ae[r]);
+                ao[r] = fma_bf16<1, 1>(m[1], X1.x, ao[r]);
+                ae[r] = fma_bf16<1, 0>(m[2], X1.y, ae[r]);
+                ao[r] = fma_bf16<1, 1>(m[3], X1.y, ao[r]);
+                ae[r] = fma_bf16<1, 0>(m[4], X1.z, ae[r]);
+                ao[r] = fma_bf16<1, 1>(m[5], X1.z, ao[r]);
+                ae[r] = fma_bf16<1, 0>(m[6], X1.w, ae[r]);
+                ao[r] = fma_bf16<1, 1>(m[7], X1.w, ao[r]);
+            }
         }
     }
 }
@@ -375,9 +449,9 @@ __device__ __forceinline__ void subgroup_dot_vp_smem(uint32_t wcell, uint32_t xs
 
 // Step 2: the subgroup's term from its pair sums.
 template <bool STREAMED>
-__device__ __forceinline__ float subgroup_term(uint64_t acc, float s, float b, float sx, float f1, float f2)
+__device__ __forceinline__ float subgroup_term(float ae, float ao, float s, float b, float sx, float f1, float f2)
 {
-    float d = __fadd_rn(pair_lo(acc), pair_hi(acc));
+    float d = __fadd_rn(ae, ao);
     d = __fmul_rn(__fmul_rn(d, f1), f2);
 #if defined(QMV_TEST_MUTATE_ORDER)
     // Test-only build: the streamed kernel adds the bias term last instead, a
@@ -431,8 +505,11 @@ struct Traits {
 
 // Stages x of subgroups [sub_lo, sub_lo + nsub) of every vector at smem + xs_off
 // (steps 1 and 2 of the fixed order): eight threads per subgroup, eight
-// elements each; threads [0, nthreads) of the CTA take part.
-template <int BITS, int V>
+// elements each; threads [0, nthreads) of the CTA take part. Each subgroup is
+// kXsB16 bytes: its 64 bf16 x' (octets in processing order), then
+// (sx, f1, f2, 0) as floats. BF16_FIELDS selects the scaling of the bf16
+// field reading (x''), else that of the fp32 field reading (x').
+template <int BITS, int V, bool BF16_FIELDS>
 __device__ __forceinline__ void stage_x(uint8_t *smem, int xs_off, const uint16_t *x, int K, int sub_lo, int nsub,
                                         int nsub_max, int tid, int nthreads)
 {
@@ -461,16 +538,21 @@ __device__ __forceinline__ void stage_x(uint8_t *smem, int xs_off, const uint16_
             const uint32_t o = __shfl_xor_sync(0xffffffffu, e, m);
             e = o > e ? o : e;
         }
-        // x' = x * 2^(254 - bits*k - E), as two exact power-of-two factors
+        // x' = x * 2^(254 - bits*k - E) (k: position in the 16-bit half) or
+        // x'' = x * 2^(238 - bits*j - E) (j: position in the byte), as two
+        // exact power-of-two factors; elements more than 231 binades below
+        // E become a zero of their sign
         float xr[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int k = BITS == 4 ? (i & 3) : i;
-            const int pw = 254 - BITS * k - int(e);
+            const int k = BF16_FIELDS ? (BITS == 4 ? (i & 1) : (i & 3)) : (BITS == 4 ? (i & 3) : i);
+            const int pw = (BF16_FIELDS ? 238 : 254) - BITS * k - int(e);
             const int p1 = pw < 127 ? pw : 127;
             const float m1 = __uint_as_float(uint32_t(p1 + 127) << 23);
             const float m2 = __uint_as_float(uint32_t(pw - p1 + 127) << 23);
-            xr[i] = bf16_round(__fmul_rn(__fmul_rn(xv[i], m1), m2));
+            const uint32_t xb = __float_as_uint(xv[i]);
+            xr[i] = int(e) - int((xb >> 23) & 0xFFu) > 231 ? __uint_as_float(xb & 0x80000000u)
+                                                            : bf16_round(__fmul_rn(__fmul_rn(xv[i], m1), m2));
         }
         // eight-element sum, left to right; the subgroup's sum gathers the eight in order
         float s8 = xv[0];
@@ -486,27 +568,18 @@ __device__ __forceinline__ void stage_x(uint8_t *smem, int xs_off, const uint16_
             // octet position of these eight elements in processing order
             const int t = sub_lo + sl;
             const int oct = BITS == 4 ? (e8 ^ (((t >> 2) & 1) * 4)) : e8;
-            if constexpr (V == 1) {
-                float4 *dst = reinterpret_cast<float4 *>(smem + xs_off + size_t(sl) * kXsF32 * 4 + oct * 32);
-                dst[0] = make_float4(xr[0], xr[1], xr[2], xr[3]);
-                dst[1] = make_float4(xr[4], xr[5], xr[6], xr[7]);
-            } else {
-                uint32_t pk[4];
+            uint32_t pk[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    pk[i] = (__float_as_uint(xr[2 * i]) >> 16) | (__float_as_uint(xr[2 * i + 1]) & 0xFFFF0000u);
-                *reinterpret_cast<uint4 *>(smem + xs_off + (size_t(v) * nsub_max + sl) * kXsB16 + oct * 16) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            }
+            for (int i = 0; i < 4; ++i)
+                pk[i] = (__float_as_uint(xr[2 * i]) >> 16) | (__float_as_uint(xr[2 * i + 1]) & 0xFFFF0000u);
+            *reinterpret_cast<uint4 *>(smem + xs_off + (size_t(v) * nsub_max + sl) * kXsB16 + oct * 16) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
             if (e8 == 0) {
                 const int c = int(e) - 105;  // f1 * f2 = 2^c
                 const int c1 = c < 127 ? c : 127;
                 const float4 meta = make_float4(sx, __uint_as_float(uint32_t(c1 + 127) << 23),
                                                 __uint_as_float(uint32_t(c - c1 + 127) << 23), 0.0f);
-                if constexpr (V == 1)
-                    *reinterpret_cast<float4 *>(smem + xs_off + size_t(sl) * kXsF32 * 4 + 256) = meta;
-                else
-                    *reinterpret_cast<float4 *>(smem + xs_off + (size_t(v) * nsub_max + sl) * kXsB16 + 128) = meta;
+                *reinterpret_cast<float4 *>(smem + xs_off + (size_t(v) * nsub_max + sl) * kXsB16 + 128) = meta;
             }
         }
     }
@@ -519,13 +592,13 @@ template <int BITS>
 __device__ __forceinline__ float chunk_v1(const uint4 (&quads)[kRows][BITS == 4 ? 2 : 1], uint32_t xsub,
                                           const float (&fs)[kRows], const float (&fb)[kRows], bool active, int lane)
 {
-    uint64_t acc[kRows];
-    subgroup_dot_v1<BITS>(quads, xsub, acc);
-    const float4 meta = lds_f4(xsub + 256);
+    float ae[kRows], ao[kRows];
+    subgroup_dot_v1<BITS>(quads, xsub, ae, ao);
+    const float4 meta = lds_f4(xsub + 128);
     float val[4];
 #pragma unroll
     for (int r = 0; r < kRows; ++r) {
-        const float term = subgroup_term<false>(acc[r], fs[r], fb[r], meta.x, meta.y, meta.z);
+        const float term = subgroup_term<false>(ae[r], ao[r], fs[r], fb[r], meta.x, meta.y, meta.z);
         val[r] = active ? term : 0.0f;
     }
     return tree_reduce_scatter<4>(val, lane);
@@ -737,7 +810,7 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_s, const CU
     } else {
         // --------------------------------------------------------- consumers
         grid_dependency_wait();  // x may be written by the preceding grid
-        stage_x<BITS, 1>(smem, L.xs, p.x, p.K, sub_lo, nsub, nsub_max, tid, C * 32);
+        stage_x<BITS, 1, true>(smem, L.xs, p.x, p.K, sub_lo, nsub, nsub_max, tid, C * 32);
         asm volatile("bar.sync 1, %0;" ::"r"(C * 32) : "memory");  // consumer warps only
 
         uint32_t poff[NP];
@@ -799,7 +872,7 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_s, const CU
                     fb[r] = bf16_bits_to_f32(lds_u16(ba[r] + gi2));
                 }
                 const float tot =
-                    chunk_v1<BITS>(quads, xs + uint32_t(tl - sub_lo) * kXsF32 * 4, fs, fb, active, lane);
+                    chunk_v1<BITS>(quads, xs + uint32_t(tl - sub_lo) * kXsB16, fs, fb, active, lane);
                 const int r = lane >> 3;
                 if ((lane & 7) == 0 && r < g.nr) cvs[(g.r0 - row_t0 + r) * cpc_here + (cc - c_lo)] = tot;
             }
@@ -905,7 +978,7 @@ __device__ __forceinline__ void qmv_direct_body(const Params &p)
     if (u0 < nunits) load_unit(u0, w_cur, s_cur, b_cur);
     grid_launch_dependents();
     grid_dependency_wait();  // x may be written by the preceding grid
-    stage_x<BITS, V>(smem, L.xs, p.x, p.K, sub_lo, nsub, nsub_max, tid, nthreads);
+    stage_x<BITS, V, false>(smem, L.xs, p.x, p.K, sub_lo, nsub, nsub_max, tid, nthreads);
     __syncthreads();
 
     const uint32_t xv_bytes = uint32_t(nsub_max) * kXsB16;
@@ -946,7 +1019,7 @@ __device__ __forceinline__ void qmv_direct_body(const Params &p)
                 const float4 meta = lds_f4(xsub + v * xv_bytes + 128);
 #pragma unroll
                 for (int r = 0; r < kRows; ++r) {
-                    const float term = subgroup_term<true>(acc[r][v], fs[r], fb[r], meta.x, meta.y, meta.z);
+                    const float term = subgroup_term<true>(pair_lo(acc[r][v]), pair_hi(acc[r][v]), fs[r], fb[r], meta.x, meta.y, meta.z);
                     val[r * T::VP + v] = active ? term : 0.0f;
                 }
             }

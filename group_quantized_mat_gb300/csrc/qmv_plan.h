@@ -16,8 +16,7 @@ constexpr int kChunkSubs = 32;      // subgroups per chunk, one per lane of a wa
 constexpr int kChunkElems = kSub * kChunkSubs;
 constexpr int kRows = 4;            // rows per work unit; every lane of the warp works on all of them
 constexpr int kMaxM = 16;
-constexpr int kXsF32 = 68;          // floats per staged subgroup, fp32 layout: 64 x' + (sx, f1, f2, 0)
-constexpr int kXsB16 = 144;         // bytes per staged subgroup, bf16 layout: 128 B x' + (sx, f1, f2, 0)
+constexpr int kXsB16 = 144;         // bytes per staged subgroup: 128 B of bf16 x' + (sx, f1, f2, 0) as floats
 
 __host__ __device__ constexpr int sub_bytes(int bits) { return kSub * bits / 8; }
 __host__ __device__ constexpr int chunk_bytes(int bits) { return kChunkElems * bits / 8; }
@@ -106,7 +105,7 @@ __host__ __device__ inline RingLayout ring_layout(int pitch, int sb_mode_unit, i
     L.slot_bytes = L.sb_off + (sb_mode_unit ? 2 : 2 * kRows) * L.sbs;
     L.ring = 0;
     L.xs = slots * L.slot_bytes;
-    L.cv = align_up(L.xs + nsub * kXsF32 * 4, 16);
+    L.cv = align_up(L.xs + nsub * kXsB16, 16);
     L.bar = align_up(L.cv + max_rb * kRows * cpc * 4, 16);
     L.misc = L.bar + 2 * slots * 8;
     L.total = L.misc + 32 + kBoxAlign;  // next-unit counter, abort flag, issued counts; alignment slack

@@ -113,6 +113,36 @@ def test_streamed_columns_bit_identical_to_m1(N, K, bits, gs):
         assert np.array_equal(per_col.view(np.uint32), y_32.view(np.uint32))
 
 
+def _wide_range_x(M: int, K: int, seed: int) -> np.ndarray:
+    """bf16 x whose subgroups mix a large element with ones up to 240 binades
+    smaller, around the point (231 binades) past which the staging makes an
+    element a zero of its sign."""
+    rng = np.random.default_rng(seed)
+    top = rng.integers(236, 246, size=(M, K // 64))
+    gap = rng.choice(np.array([0, 1, 3, 7, 100, 200, 228, 229, 230, 231, 232, 233, 234, 236, 238, 240]), size=(M, K))
+    ex = np.clip(np.repeat(top, 64, axis=1) - gap, 0, 254)
+    ex[:, ::64] = np.repeat(top[:, :, None], 1, axis=2)[:, :, 0]   # the subgroup's largest
+    mant = rng.integers(0, 128, size=(M, K))
+    sign = rng.integers(0, 2, size=(M, K))
+    return ((sign << 15) | (ex << 7) | mant).astype(np.uint16)
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_wide_exponent_range(o, bits):
+    """Subgroups spanning more than 231 binades: the two field readings still
+    agree bit for bit, and the result stays within the tolerance."""
+    N, K = 96, 4096
+    inp = synth.make_inputs(N, K, 6, bits, 64, seed=31)
+    inp.x = _wide_range_x(6, K, 5 + bits)
+    dp = DeviceProblem(inp)
+    y6 = dp.run(flags=g.F32_OUT)
+    singles = np.stack([dp.run(x=dp.x[m:m + 1].contiguous(), M=1, flags=g.F32_OUT)[0] for m in range(6)])
+    assert np.array_equal(y6.view(np.uint32), singles.view(np.uint32))
+    assert np.array_equal(dp.run(), np.stack([dp.run(x=dp.x[m:m + 1].contiguous(), M=1)[0] for m in range(6)]))
+    ref, terms = oracle_rows(o, inp)
+    assert np.all(np.abs(y6 - ref) <= 1e-4 * terms + 1e-6)
+
+
 def test_position_invariance():
     inp = synth.make_inputs(3840, 3840, 13, 4, 64, seed=11)
     dp = DeviceProblem(inp)
