@@ -8,6 +8,7 @@
 
 #include <cstdint>
 #include <cstdio>
+#include <cstring>
 #include <mutex>
 
 #include "qmv.h"
@@ -66,7 +67,7 @@ struct Problem {
     int threads;
     int smem;       // dynamic shared memory per CTA
     // one-vector ring
-    int uc, full_rows, pitch, sb_mode_unit, sbox, slots, consumers;
+    int uc, unit_mode, pitch, sb_mode_unit, sbox, slots, consumers;
 };
 
 // Largest dynamic shared memory a CTA may use (static shared memory and
@@ -141,8 +142,10 @@ Problem plan_direct(int V, int N, int K, int bits, int gs, int sms)
 
 // One-vector kernel: chunks per CTA from the staged-x budget (all of K when
 // it fits), units (whole rows in one copy when four rows fit kUnitMax, else
-// uc chunks of each row), scale/bias boxes, then as many ring slots as fit
-// (a multiple of the producer warps, at most kMaxSlots and the CTA's units).
+// uc chunks of each row: one 2-D box of the 4 rows when the scale/bias rows
+// are 16-byte multiples, else one copy per row), scale/bias boxes, then as
+// many ring slots as fit (a multiple of the producer warps, at most kMaxSlots
+// and the CTA's units).
 Problem plan_ring(int N, int K, int bits, int gs, int sms)
 {
     Problem pr{};
@@ -161,11 +164,12 @@ Problem plan_ring(int N, int K, int bits, int gs, int sms)
     if (g_tune.uc > 0) whole = false;
 #endif
     if (whole) {
-        pr.full_rows = 1;
+        pr.unit_mode = qmv::kUnitRows;
         pr.uc = pr.ks;
         pr.pitch = pr.row_bytes;
     } else {
-        pr.full_rows = 0;
+        // a tile row is at most 256 eight-byte elements (kUnitMax / 4 rows)
+        pr.unit_mode = pr.G % 8 == 0 ? qmv::kUnitTiles : qmv::kUnitPieces;
         pr.uc = kUnitMax / (qmv::kRows * cb);
         if (pr.uc < 1) pr.uc = 1;
         if (pr.uc > pr.cpc) pr.uc = pr.cpc;
@@ -177,8 +181,13 @@ Problem plan_ring(int N, int K, int bits, int gs, int sms)
     // Scale/bias boxes: one per unit when the four rows' groups fit one box,
     // else one per row. A box starts at a multiple of 8 elements, so it spans
     // up to 7 more.
-    const int gpu = pr.full_rows ? pr.G : (pr.uc * qmv::kChunkElems / gs < pr.G ? pr.uc * qmv::kChunkElems / gs : pr.G);
-    if (pr.full_rows && qmv::kRows * pr.G + 7 <= 256) {
+    const int gpu = pr.unit_mode == qmv::kUnitRows
+                        ? pr.G
+                        : (pr.uc * qmv::kChunkElems / gs < pr.G ? pr.uc * qmv::kChunkElems / gs : pr.G);
+    if (pr.unit_mode == qmv::kUnitTiles) {
+        pr.sb_mode_unit = 1;
+        pr.sbox = qmv::kRows * (pr.uc * qmv::kChunkElems / gs);  // 4 box rows, each the unit's groups
+    } else if (pr.unit_mode == qmv::kUnitRows && qmv::kRows * pr.G + 7 <= 256) {
         pr.sb_mode_unit = 1;
         pr.sbox = qmv::align_up(qmv::kRows * pr.G + 7, 8);
     } else {
@@ -233,20 +242,48 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// Scales or biases as a 1-D bf16 tensor of N*G elements; one box is `sbox`
-// elements. Elements past the end arrive as zeros.
+// Scales or biases: for tiles a 2-D bf16 tensor [N][G] whose box is 4 rows
+// of sbox / 4 groups, else a 1-D tensor of N*G elements whose box is `sbox`
+// elements. Elements outside the tensor arrive as zeros.
 int encode_sb_map(CUtensorMap *map, const uint16_t *base, const Problem &pr)
 {
     auto fn = encode_fn();
     if (!fn) return -1;
-    const cuuint64_t dims[1] = {cuuint64_t(pr.N) * cuuint64_t(pr.G)};
-    const cuuint64_t strides[1] = {0};
-    const cuuint32_t box[1] = {cuuint32_t(pr.sbox)};
-    const cuuint32_t estr[1] = {1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 1, const_cast<uint16_t *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r;
+    if (pr.unit_mode == qmv::kUnitTiles) {
+        const cuuint64_t dims[2] = {cuuint64_t(pr.G), cuuint64_t(pr.N)};
+        const cuuint64_t strides[1] = {cuuint64_t(pr.G) * 2};  // a multiple of 16 bytes (G % 8 == 0)
+        const cuuint32_t box[2] = {cuuint32_t(pr.sbox / qmv::kRows), cuuint32_t(qmv::kRows)};
+        const cuuint32_t estr[2] = {1, 1};
+        r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        const cuuint64_t dims[1] = {cuuint64_t(pr.N) * cuuint64_t(pr.G)};
+        const cuuint64_t strides[1] = {0};
+        const cuuint32_t box[1] = {cuuint32_t(pr.sbox)};
+        const cuuint32_t estr[1] = {1};
+        r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 1, const_cast<uint16_t *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     return int(r);
+}
+
+// Packed weights as a 2-D tensor [N][row_bytes / 8] of 8-byte elements (a
+// row is a multiple of 16 bytes); a box is 4 rows of `pitch` bytes. Bytes
+// past a row's end and rows past N arrive as zeros.
+int encode_w_map(CUtensorMap *map, const uint32_t *w_q, const Problem &pr)
+{
+    auto fn = encode_fn();
+    if (!fn) return -1;
+    const cuuint64_t dims[2] = {cuuint64_t(pr.row_bytes / 8), cuuint64_t(pr.N)};
+    const cuuint64_t strides[1] = {cuuint64_t(pr.row_bytes)};
+    const cuuint32_t box[2] = {cuuint32_t(pr.pitch / 8), cuuint32_t(qmv::kRows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return int(fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint32_t *>(w_q), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
 }
 
 qmv_status sm_count(int dev, int *out)
@@ -302,8 +339,7 @@ qmv_status library_workspace(int dev, size_t need, void **out)
     return QMV_OK;
 }
 
-cudaError_t dispatch(const Problem &pr, const CUtensorMap *map_s, const CUtensorMap *map_b, const qmv::Params &p,
-                     bool pdl, cudaStream_t stream)
+cudaError_t dispatch(const Problem &pr, const qmv::RingMaps &maps, const qmv::Params &p, bool pdl, cudaStream_t stream)
 {
     qmv::Launch l;
     l.grid = dim3(pr.grid_rows, pr.nranges);
@@ -313,12 +349,12 @@ cudaError_t dispatch(const Problem &pr, const CUtensorMap *map_s, const CUtensor
     if (pr.V == 1) {
         qmv::RingParams rp;
         static_cast<qmv::Params &>(rp) = p;
-        rp.uc = pr.uc; rp.full_rows = pr.full_rows; rp.pitch = pr.pitch; rp.sb_mode_unit = pr.sb_mode_unit;
+        rp.uc = pr.uc; rp.unit_mode = pr.unit_mode; rp.pitch = pr.pitch; rp.sb_mode_unit = pr.sb_mode_unit;
         rp.sbox = pr.sbox; rp.slots = pr.slots; rp.consumers = pr.consumers;
-        if (pr.bits == 4 && pr.gs == 64) return qmv::launch_b4g64_m1(*map_s, *map_b, rp, l, stream);
-        if (pr.bits == 4 && pr.gs == 128) return qmv::launch_b4g128_m1(*map_s, *map_b, rp, l, stream);
-        if (pr.bits == 2 && pr.gs == 64) return qmv::launch_b2g64_m1(*map_s, *map_b, rp, l, stream);
-        return qmv::launch_b2g128_m1(*map_s, *map_b, rp, l, stream);
+        if (pr.bits == 4 && pr.gs == 64) return qmv::launch_b4g64_m1(maps, rp, l, stream);
+        if (pr.bits == 4 && pr.gs == 128) return qmv::launch_b4g128_m1(maps, rp, l, stream);
+        if (pr.bits == 2 && pr.gs == 64) return qmv::launch_b2g64_m1(maps, rp, l, stream);
+        return qmv::launch_b2g128_m1(maps, rp, l, stream);
     }
     if (pr.bits == 4 && pr.gs == 64) return qmv::launch_b4g64_streamed(pr.V, p, l, stream);
     if (pr.bits == 4 && pr.gs == 128) return qmv::launch_b4g128_streamed(pr.V, p, l, stream);
@@ -368,12 +404,14 @@ qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t 
     st = device_error_ptr(dev, &err);
     if (st != QMV_OK) return st;
 
-    CUtensorMap map_s, map_b;
+    qmv::RingMaps maps;
+    memset(&maps, 0, sizeof maps);
     if (V == 1) {
-        int enc = encode_sb_map(&map_s, scales, pr);
-        if (enc == 0) enc = encode_sb_map(&map_b, biases, pr);
+        int enc = encode_sb_map(&maps.s, scales, pr);
+        if (enc == 0) enc = encode_sb_map(&maps.b, biases, pr);
+        if (enc == 0 && pr.unit_mode == qmv::kUnitTiles) enc = encode_w_map(&maps.w, w_q, pr);
         if (enc != 0) {
-            snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled(scales/biases) returned %d%s", enc,
+            snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled returned %d%s", enc,
                      enc < 0 ? " (driver entry point not found)" : "");
             return QMV_ERR_CUDA;
         }
@@ -396,7 +434,7 @@ qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t 
     for (int m = 0; m < launches; ++m) {
         p.x = x + size_t(m) * K;
         p.y = static_cast<char *>(y) + size_t(m) * N * ysize;
-        ce = dispatch(pr, &map_s, &map_b, p, pdl, stream);
+        ce = dispatch(pr, maps, p, pdl, stream);
         if (ce != cudaSuccess) return cuda_fail("kernel launch", ce);
     }
     return QMV_OK;

@@ -2,10 +2,9 @@
 #include "qmv_launch.cuh"
 
 namespace qmv {
-cudaError_t launch_b4g128_m1(const CUtensorMap &map_s, const CUtensorMap &map_b, const RingParams &p, const Launch &l,
-                             cudaStream_t stream)
+cudaError_t launch_b4g128_m1(const RingMaps &maps, const RingParams &p, const Launch &l, cudaStream_t stream)
 {
-    return launch_m1<4, 128>(map_s, map_b, p, l, stream);
+    return launch_m1<4, 128>(maps, p, l, stream);
 }
 cudaError_t launch_b4g128_streamed(int V, const Params &p, const Launch &l, cudaStream_t stream)
 {

@@ -174,6 +174,14 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
+// The same without an L2 hint.
+__device__ __forceinline__ void bulk_load_plain(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 // 1-D tensor-map box load at element coordinate x (a multiple of 8 for
 // 2-byte elements); elements past the tensor's end arrive as zeros.
 __device__ __forceinline__ void tma_load_1d(uint32_t dst, const CUtensorMap *map, int x, uint32_t bar)
@@ -182,6 +190,27 @@ __device__ __forceinline__ void tma_load_1d(uint32_t dst, const CUtensorMap *map
         "cp.async.bulk.tensor.1d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2}], [%3];" ::"r"(
             dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(bar)
+        : "memory");
+}
+
+// 2-D tensor-map box load at element coordinates (x, y), x * element size a
+// multiple of 16 bytes; elements outside the tensor arrive as zeros.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar,
+                                                 uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
         : "memory");
 }
 
@@ -334,14 +363,14 @@ __device__ __forceinline__ void piece_offsets(int lane, uint32_t (&off)[BITS == 
 // Step 1 for V = 1 in the bf16 field reading: ae[r], ao[r] of the lane's
 // subgroup in rows 0..3.
 //   quads[r]  the subgroup's bytes in row r (16-byte pieces, processing order);
-//   xsub      shared address of the staged subgroup (64 bf16 x'', octets in
-//             processing order, 16 bytes each).
+//   xsub      shared address of the staged subgroup (64 bf16 x'', octet o in
+//             processing order at 16 * (o ^ sw)).
 // A 4-bit octet is one word w: fields (0,4), (1,5), (2,6), (3,7) sit in the
 // two halves of w & 0x000F000F, w & 0x00F000F0 and the same masks of w >> 8.
 // A 2-bit word holds octets 2p (low halves) and 2p + 1 (high halves): fields
 // k and k + 4 of both in the masks 3 << 2k of w and of w >> 8.
 template <int BITS>
-__device__ __forceinline__ void subgroup_dot_v1(const uint4 (&quads)[kRows][BITS == 4 ? 2 : 1], uint32_t xsub,
+__device__ __forceinline__ void subgroup_dot_v1(const uint4 (&quads)[kRows][BITS == 4 ? 2 : 1], uint32_t xsub, uint32_t sw,
                                                 float (&ae)[kRows], float (&ao)[kRows])
 {
 #pragma unroll
@@ -349,7 +378,7 @@ __device__ __forceinline__ void subgroup_dot_v1(const uint4 (&quads)[kRows][BITS
     if constexpr (BITS == 4) {
 #pragma unroll
         for (int o = 0; o < 8; ++o) {
-            const uint4 X = lds_v4_u32(xsub + o * 16);
+            const uint4 X = lds_v4_u32(xsub + ((uint32_t(o) ^ sw) << 4));
 #pragma unroll
             for (int r = 0; r < kRows; ++r) {
                 const uint32_t w = word_of(quads[r][o >> 2], o & 3), w8 = w >> 8;
@@ -368,7 +397,8 @@ __device__ __forceinline__ void subgroup_dot_v1(const uint4 (&quads)[kRows][BITS
     } else {
 #pragma unroll
         for (int pw = 0; pw < 4; ++pw) {
-            const uint4 X0 = lds_v4_u32(xsub + pw * 32), X1 = lds_v4_u32(xsub + pw * 32 + 16);
+            const uint4 X0 = lds_v4_u32(xsub + ((uint32_t(2 * pw) ^ sw) << 4));
+            const uint4 X1 = lds_v4_u32(xsub + ((uint32_t(2 * pw + 1) ^ sw) << 4));
 #pragma unroll
             for (int r = 0; r < kRows; ++r) {
                 const uint32_t w = word_of(quads[r][0], pw), w8 = w >> 8;
@@ -503,98 +533,145 @@ struct Traits {
     static constexpr int NP = BITS == 4 ? 2 : 1;              // 16-byte pieces per subgroup row
 };
 
-// Stages x of subgroups [sub_lo, sub_lo + nsub) of every vector at smem + xs_off
-// (steps 1 and 2 of the fixed order): eight threads per subgroup, eight
-// elements each; threads [0, nthreads) of the CTA take part. Each subgroup is
-// kXsB16 bytes: its 64 bf16 x' (octets in processing order), then
-// (sx, f1, f2, 0) as floats. BF16_FIELDS selects the scaling of the bf16
-// field reading (x''), else that of the fp32 field reading (x').
-template <int BITS, int V, bool BF16_FIELDS>
+// Steps 1 and 2 for eight consecutive elements of a subgroup, held as raw
+// bf16 by each of eight consecutive lanes (all 32 lanes of the warp call
+// this): their staged x' as four bf16 pairs, and the subgroup's
+// (sx, f1, f2, 0). BF16_FIELDS selects the scaling of the bf16 field reading
+// (x''), else that of the fp32 field reading (x').
+template <int BITS, bool BF16_FIELDS>
+__device__ __forceinline__ void stage_eight(const uint4 &raw, uint4 &packed, float4 &meta)
+{
+    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t e = 1;
+    float xv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t bits = (i & 1) ? (w4[i / 2] >> 16) : (w4[i / 2] & 0xFFFFu);
+        xv[i] = bf16_bits_to_f32(bits);
+        const uint32_t f = (bits >> 7) & 0xFFu;
+        e = f > e ? f : e;
+    }
+    // largest exponent field of the subgroup
+#pragma unroll
+    for (int m = 1; m < 8; m <<= 1) {
+        const uint32_t o = __shfl_xor_sync(0xffffffffu, e, m);
+        e = o > e ? o : e;
+    }
+    // x' = x * 2^(254 - bits*k - E) (k: position in the 16-bit half) or
+    // x'' = x * 2^(238 - bits*j - E) (j: position in the byte), as two
+    // exact power-of-two factors; elements more than 231 binades below
+    // E become a zero of their sign
+    float xr[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int k = BF16_FIELDS ? (BITS == 4 ? (i & 1) : (i & 3)) : (BITS == 4 ? (i & 3) : i);
+        const int pw = (BF16_FIELDS ? 238 : 254) - BITS * k - int(e);
+        const int p1 = pw < 127 ? pw : 127;
+        const float m1 = __uint_as_float(uint32_t(p1 + 127) << 23);
+        const float m2 = __uint_as_float(uint32_t(pw - p1 + 127) << 23);
+        const uint32_t xb = __float_as_uint(xv[i]);
+        xr[i] = int(e) - int((xb >> 23) & 0xFFu) > 231 ? __uint_as_float(xb & 0x80000000u)
+                                                        : bf16_round(__fmul_rn(__fmul_rn(xv[i], m1), m2));
+    }
+    uint32_t pk[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        pk[i] = (__float_as_uint(xr[2 * i]) >> 16) | (__float_as_uint(xr[2 * i + 1]) & 0xFFFF0000u);
+    packed = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    // eight-element sum, left to right; the subgroup's sum gathers the eight in order
+    float s8 = xv[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) s8 = __fadd_rn(s8, xv[i]);
+    float sx = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float o = __shfl_sync(0xffffffffu, s8, i, 8);
+        sx = i == 0 ? o : __fadd_rn(sx, o);
+    }
+    const int c = int(e) - 105;  // f1 * f2 = 2^c
+    const int c1 = c < 127 ? c : 127;
+    meta = make_float4(sx, __uint_as_float(uint32_t(c1 + 127) << 23), __uint_as_float(uint32_t(c - c1 + 127) << 23),
+                       0.0f);
+}
+
+// Octet position of eighth e8 of subgroup t in processing order.
+template <int BITS>
+__device__ __forceinline__ int octet_position(int t, int e8)
+{
+    return BITS == 4 ? (e8 ^ (((t >> 2) & 1) * 4)) : e8;
+}
+
+// Stages x of subgroups [sub_lo, sub_lo + nsub) of every vector at smem + xs_off,
+// loading it from global memory (the streamed kernel): eight threads per
+// subgroup, eight elements each; threads [0, nthreads) of the CTA take part.
+// Each subgroup is kXsB16 bytes: its 64 bf16 x' (octets in processing order),
+// then (sx, f1, f2, 0) as floats.
+template <int BITS, int V>
 __device__ __forceinline__ void stage_x(uint8_t *smem, int xs_off, const uint16_t *x, int K, int sub_lo, int nsub,
                                         int nsub_max, int tid, int nthreads)
 {
     const int per_vec = nsub * 8, all = V * per_vec;
     const int all_pad = (all + nthreads - 1) / nthreads * nthreads;
     for (int u = tid; u < all_pad; u += nthreads) {
-        const bool live = u < all;
+        const bool live = u < all;  // uniform over each eight-lane group
         const int v = live ? u / per_vec : 0;
         const int rem = live ? u - v * per_vec : 0;
         const int sl = rem >> 3, e8 = rem & 7;  // subgroup (CTA-local), eighth
         uint4 raw = make_uint4(0, 0, 0, 0);
         if (live) raw = __ldg(reinterpret_cast<const uint4 *>(x + size_t(v) * K + size_t(sub_lo + sl) * kSub) + e8);
-        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-        uint32_t e = 1;
-        float xv[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t bits = (i & 1) ? (w4[i / 2] >> 16) : (w4[i / 2] & 0xFFFFu);
-            xv[i] = bf16_bits_to_f32(bits);
-            const uint32_t f = (bits >> 7) & 0xFFu;
-            e = f > e ? f : e;
-        }
-        // largest exponent field of the subgroup (its eight threads are eight consecutive lanes)
-#pragma unroll
-        for (int m = 1; m < 8; m <<= 1) {
-            const uint32_t o = __shfl_xor_sync(0xffffffffu, e, m);
-            e = o > e ? o : e;
-        }
-        // x' = x * 2^(254 - bits*k - E) (k: position in the 16-bit half) or
-        // x'' = x * 2^(238 - bits*j - E) (j: position in the byte), as two
-        // exact power-of-two factors; elements more than 231 binades below
-        // E become a zero of their sign
-        float xr[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int k = BF16_FIELDS ? (BITS == 4 ? (i & 1) : (i & 3)) : (BITS == 4 ? (i & 3) : i);
-            const int pw = (BF16_FIELDS ? 238 : 254) - BITS * k - int(e);
-            const int p1 = pw < 127 ? pw : 127;
-            const float m1 = __uint_as_float(uint32_t(p1 + 127) << 23);
-            const float m2 = __uint_as_float(uint32_t(pw - p1 + 127) << 23);
-            const uint32_t xb = __float_as_uint(xv[i]);
-            xr[i] = int(e) - int((xb >> 23) & 0xFFu) > 231 ? __uint_as_float(xb & 0x80000000u)
-                                                            : bf16_round(__fmul_rn(__fmul_rn(xv[i], m1), m2));
-        }
-        // eight-element sum, left to right; the subgroup's sum gathers the eight in order
-        float s8 = xv[0];
-#pragma unroll
-        for (int i = 1; i < 8; ++i) s8 = __fadd_rn(s8, xv[i]);
-        float sx = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float o = __shfl_sync(0xffffffffu, s8, i, 8);
-            sx = i == 0 ? o : __fadd_rn(sx, o);
-        }
+        uint4 packed;
+        float4 meta;
+        stage_eight<BITS, false>(raw, packed, meta);
         if (live) {
-            // octet position of these eight elements in processing order
-            const int t = sub_lo + sl;
-            const int oct = BITS == 4 ? (e8 ^ (((t >> 2) & 1) * 4)) : e8;
-            uint32_t pk[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                pk[i] = (__float_as_uint(xr[2 * i]) >> 16) | (__float_as_uint(xr[2 * i + 1]) & 0xFFFF0000u);
-            *reinterpret_cast<uint4 *>(smem + xs_off + (size_t(v) * nsub_max + sl) * kXsB16 + oct * 16) =
-                make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            if (e8 == 0) {
-                const int c = int(e) - 105;  // f1 * f2 = 2^c
-                const int c1 = c < 127 ? c : 127;
-                const float4 meta = make_float4(sx, __uint_as_float(uint32_t(c1 + 127) << 23),
-                                                __uint_as_float(uint32_t(c - c1 + 127) << 23), 0.0f);
-                *reinterpret_cast<float4 *>(smem + xs_off + (size_t(v) * nsub_max + sl) * kXsB16 + 128) = meta;
-            }
+            uint8_t *cell = smem + xs_off + (size_t(v) * nsub_max + sl) * kXsB16;
+            *reinterpret_cast<uint4 *>(cell + octet_position<BITS>(sub_lo + sl, e8) * 16) = packed;
+            if (e8 == 0) *reinterpret_cast<float4 *>(cell + 128) = meta;
+        }
+    }
+}
+
+// Stages x (one vector) for the one-vector kernel in place: the raw bf16 x of
+// subgroups [sub_lo, sub_lo + nsub) lies densely at xs (128 bytes a
+// subgroup); subgroup sl's x'' replaces its raw bytes, octet o stored at
+// 16 * (o ^ (sl & 7)) (eight consecutive subgroups then read the same octet
+// from eight different bank groups), and its (sx, f1, f2, 0) goes to
+// xm + 16 * sl. The eight lanes of a subgroup read their raw bytes before the
+// shuffles of stage_eight and write only inside that subgroup, so no lane
+// overwrites bytes another lane has yet to read.
+template <int BITS>
+__device__ __forceinline__ void stage_x_ring(uint32_t xs, uint32_t xm, int sub_lo, int nsub, int tid, int nthreads)
+{
+    const int all = nsub * 8;
+    const int all_pad = (all + nthreads - 1) / nthreads * nthreads;
+    for (int u = tid; u < all_pad; u += nthreads) {
+        const bool live = u < all;  // uniform over each eight-lane group
+        const int sl = live ? u >> 3 : 0, e8 = u & 7;
+        const uint32_t cell = xs + uint32_t(sl) * 128u;
+        uint4 raw = make_uint4(0, 0, 0, 0);
+        if (live) raw = lds_v4_u32(cell + uint32_t(e8) * 16u);
+        uint4 packed;
+        float4 meta;
+        stage_eight<BITS, true>(raw, packed, meta);
+        if (live) {
+            sts_v4_u32(cell + uint32_t(octet_position<BITS>(sub_lo + sl, e8) ^ (sl & 7)) * 16u, packed);
+            if (e8 == 0) sts_v4_u32(xm + uint32_t(sl) * 16u, make_uint4(__float_as_uint(meta.x), __float_as_uint(meta.y),
+                                                                       __float_as_uint(meta.z), 0u));
         }
     }
 }
 
 // One chunk of one vector for 4 rows (steps 1 to 3): the lane's subgroup
-// from `quads`, x' of subgroup `sl` at xsub; returns the chunk value of row
+// from `quads`, its x'' at xsub (swizzle sw) and (sx, f1, f2) at xmeta;
+// returns the chunk value of row
 // lane >> 3 (all lanes of that row's eight-lane group hold it).
 template <int BITS>
-__device__ __forceinline__ float chunk_v1(const uint4 (&quads)[kRows][BITS == 4 ? 2 : 1], uint32_t xsub,
-                                          const float (&fs)[kRows], const float (&fb)[kRows], bool active, int lane)
+__device__ __forceinline__ float chunk_v1(const uint4 (&quads)[kRows][BITS == 4 ? 2 : 1], uint32_t xsub, uint32_t sw,
+                                          uint32_t xmeta, const float (&fs)[kRows], const float (&fb)[kRows], bool active,
+                                          int lane)
 {
     float ae[kRows], ao[kRows];
-    subgroup_dot_v1<BITS>(quads, xsub, ae, ao);
-    const float4 meta = lds_f4(xsub + 128);
+    subgroup_dot_v1<BITS>(quads, xsub, sw, ae, ao);
+    const float4 meta = lds_f4(xmeta);
     float val[4];
 #pragma unroll
     for (int r = 0; r < kRows; ++r) {
@@ -664,7 +741,8 @@ __device__ __forceinline__ void fold_chunks(const float *cvs, int nrows, int row
 // ------------------------------------------------------- one vector: ring --
 
 template <int BITS, int GS>
-__device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_s, const CUtensorMap *map_b, const RingParams &p)
+__device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CUtensorMap *map_s, const CUtensorMap *map_b,
+                                              const RingParams &p)
 {
     constexpr int kSubB = sub_bytes(BITS);
     constexpr int kChunkB = chunk_bytes(BITS);
@@ -693,14 +771,14 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_s, const CU
     const int nsub_max = p.cpc * kChunkSubs < p.S_row ? p.cpc * kChunkSubs : p.S_row;
     const RingLayout L = ring_layout(p.pitch, p.sb_mode_unit, p.sbox, p.slots, nsub_max, p.max_rb, p.cpc);
     const uint32_t ring = smem_u32(smem + L.ring);
-    const uint32_t xs = smem_u32(smem + L.xs);
+    const uint32_t xs = smem_u32(smem + L.xs), xm = smem_u32(smem + L.xm);
     float *cvs = reinterpret_cast<float *>(smem + L.cv);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar);  // full[slots], empty[slots]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar);  // full[slots], empty[slots], x
     unsigned *s_next = reinterpret_cast<unsigned *>(smem + L.misc);
     volatile unsigned *s_abort = s_next + 1;
     // s_issued[k]: units issued by producer k (it issues k, k + P, ...).
     volatile int *s_issued = reinterpret_cast<volatile int *>(s_next + 2);
-    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + p.slots);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + p.slots), xbar = smem_u32(bars + 2 * p.slots);
 
     // Geometry of unit u: rows [r0, r0 + nr), chunks [c0, c1).
     struct Unit {
@@ -728,10 +806,18 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_s, const CU
         const int e0 = g.c0 * kChunkElems;
         const int e1 = g.c1 * kChunkElems < p.K ? g.c1 * kChunkElems : p.K;
         const uint32_t seg = uint32_t(e1 - e0) * BITS / 8;
+        if (p.unit_mode == kUnitTiles) {
+            // boxes of 4 rows: rows past N and bytes past the row's end arrive as zeros
+            mbar_arrive_expect_tx(full, uint32_t(kRows * p.pitch + 2 * p.sbox * 2));
+            tma_load_2d_hint(base, map_w, g.c0 * (kChunkB / 8), g.r0, full, pol);
+            tma_load_2d(base + L.sb_off, map_s, g.c0 * (kChunkElems / GS), g.r0, full);
+            tma_load_2d(base + L.sb_off + L.sbs, map_b, g.c0 * (kChunkElems / GS), g.r0, full);
+            return;
+        }
         const int nbox = p.sb_mode_unit ? 1 : g.nr;
-        const uint32_t wbytes = p.full_rows ? uint32_t(g.nr) * uint32_t(p.row_bytes) : uint32_t(g.nr) * seg;
+        const uint32_t wbytes = p.unit_mode == kUnitRows ? uint32_t(g.nr) * uint32_t(p.row_bytes) : uint32_t(g.nr) * seg;
         mbar_arrive_expect_tx(full, wbytes + uint32_t(2 * nbox * p.sbox * 2));
-        if (p.full_rows) {
+        if (p.unit_mode == kUnitRows) {
             bulk_load(base, p.w + size_t(g.r0) * p.row_bytes, wbytes, full, pol);
         } else {
             for (int r = 0; r < g.nr; ++r)
@@ -751,7 +837,7 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_s, const CU
         if (tid == 0) atomicOr(p.err, 2u);
         return;
     }
-    if (tid < 2 * p.slots) {  // full[] and empty[] are contiguous
+    if (tid < 2 * p.slots + 1) {  // full[], empty[] and the x barrier are contiguous
         mbar_init(full0 + 8 * tid, 1);
         fence_mbar_init();
     }
@@ -810,7 +896,16 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_s, const CU
     } else {
         // --------------------------------------------------------- consumers
         grid_dependency_wait();  // x may be written by the preceding grid
-        stage_x<BITS, 1, true>(smem, L.xs, p.x, p.K, sub_lo, nsub, nsub_max, tid, C * 32);
+        if (tid == 0) {
+            // the CTA's x range in one copy, landing where it is staged
+            mbar_arrive_expect_tx(xbar, uint32_t(nsub) * 128u);
+            bulk_load_plain(xs, p.x + size_t(sub_lo) * kSub, uint32_t(nsub) * 128u, xbar);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(xbar, 0)) && lane == 0) {
+            atomicOr(p.err, 1u);
+            *s_abort = 1;
+        }
+        stage_x_ring<BITS>(xs, xm, sub_lo, nsub, tid, C * 32);
         asm volatile("bar.sync 1, %0;" ::"r"(C * 32) : "memory");  // consumer warps only
 
         uint32_t poff[NP];
@@ -841,7 +936,15 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_s, const CU
             // Per-unit shared addresses of row r's scale / bias of group 0 of
             // the row (rows past N alias row 0).
             uint32_t sa[kRows], ba[kRows];
-            {
+            if (p.unit_mode == kUnitTiles) {
+                // box rows of sbox / 4 groups starting at the unit's first group
+                const int gb = p.sbox / kRows, g0 = g.c0 * (kChunkElems / GS);
+#pragma unroll
+                for (int r = 0; r < kRows; ++r) {
+                    sa[r] = base + L.sb_off + uint32_t(2 * (r * gb - g0));
+                    ba[r] = sa[r] + L.sbs;
+                }
+            } else {
                 const int g0 = g.c0 * (kChunkElems / GS);
 #pragma unroll
                 for (int r = 0; r < kRows; ++r) {
@@ -871,8 +974,8 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_s, const CU
                     fs[r] = bf16_bits_to_f32(lds_u16(sa[r] + gi2));
                     fb[r] = bf16_bits_to_f32(lds_u16(ba[r] + gi2));
                 }
-                const float tot =
-                    chunk_v1<BITS>(quads, xs + uint32_t(tl - sub_lo) * kXsB16, fs, fb, active, lane);
+                const uint32_t sl = uint32_t(tl - sub_lo);
+                const float tot = chunk_v1<BITS>(quads, xs + sl * 128u, sl & 7u, xm + sl * 16u, fs, fb, active, lane);
                 const int r = lane >> 3;
                 if ((lane & 7) == 0 && r < g.nr) cvs[(g.r0 - row_t0 + r) * cpc_here + (cc - c_lo)] = tot;
             }
@@ -889,6 +992,7 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_s, const CU
             for (int u = hi - p.slots > kp ? hi - p.slots : kp; u < hi; u += P)
                 (void)mbar_wait_bounded(full0 + 8 * (u % p.slots), (u / p.slots) & 1);
         }
+        if (tid == 0) (void)mbar_wait_bounded(xbar, 0);  // the x copy
         __syncthreads();
         return;
     }
@@ -978,7 +1082,7 @@ __device__ __forceinline__ void qmv_direct_body(const Params &p)
     if (u0 < nunits) load_unit(u0, w_cur, s_cur, b_cur);
     grid_launch_dependents();
     grid_dependency_wait();  // x may be written by the preceding grid
-    stage_x<BITS, V, false>(smem, L.xs, p.x, p.K, sub_lo, nsub, nsub_max, tid, nthreads);
+    stage_x<BITS, V>(smem, L.xs, p.x, p.K, sub_lo, nsub, nsub_max, tid, nthreads);
     __syncthreads();
 
     const uint32_t xv_bytes = uint32_t(nsub_max) * kXsB16;
@@ -1051,9 +1155,10 @@ constexpr int kThreadsVN = 12 * 32;
 
 template <int BITS, int GS>
 __global__ void __launch_bounds__(kThreadsV1, 1)
-    qmv_m1(const __grid_constant__ CUtensorMap map_s, const __grid_constant__ CUtensorMap map_b, const RingParams p)
+    qmv_m1(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_s,
+           const __grid_constant__ CUtensorMap map_b, const RingParams p)
 {
-    qmv_ring_body<BITS, GS>(&map_s, &map_b, p);
+    qmv_ring_body<BITS, GS>(&map_w, &map_s, &map_b, p);
 }
 
 template <int BITS, int GS, int V>

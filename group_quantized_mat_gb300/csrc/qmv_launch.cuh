@@ -41,11 +41,10 @@ cudaError_t launch_one(Kern kern, int (&configured)[64], const Launch &l, cudaSt
 }
 
 template <int BITS, int GS>
-cudaError_t launch_m1(const CUtensorMap &map_s, const CUtensorMap &map_b, const RingParams &p, const Launch &l,
-                      cudaStream_t stream)
+cudaError_t launch_m1(const RingMaps &maps, const RingParams &p, const Launch &l, cudaStream_t stream)
 {
     static int configured[64] = {0};
-    return launch_one(qmv_m1<BITS, GS>, configured, l, stream, map_s, map_b, p);
+    return launch_one(qmv_m1<BITS, GS>, configured, l, stream, maps.w, maps.s, maps.b, p);
 }
 
 template <int BITS, int GS, int V>

@@ -14,6 +14,11 @@ constexpr int kStreamedWarps = 12;
 constexpr int kRingConsumers = 16;
 constexpr int kRingProducers = 4;
 
+// Tensor maps of the one-vector kernel: weights (tiles only), scales, biases.
+struct RingMaps {
+    CUtensorMap w, s, b;
+};
+
 struct Launch {
     dim3 grid;
     int threads;
@@ -22,8 +27,7 @@ struct Launch {
 };
 
 #define QMV_DECLARE_LAUNCH(name)                                                                                  \
-    cudaError_t name##_m1(const CUtensorMap &map_s, const CUtensorMap &map_b, const RingParams &p, const Launch &l, \
-                          cudaStream_t stream);                                                                   \
+    cudaError_t name##_m1(const RingMaps &maps, const RingParams &p, const Launch &l, cudaStream_t stream);      \
     cudaError_t name##_streamed(int V, const Params &p, const Launch &l, cudaStream_t stream);
 QMV_DECLARE_LAUNCH(launch_b4g64)
 QMV_DECLARE_LAUNCH(launch_b4g128)

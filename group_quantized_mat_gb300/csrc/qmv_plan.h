@@ -55,12 +55,16 @@ struct Params {
 // being uc consecutive chunks of the CTA's range; producer warps stream them
 // through `slots` shared-memory slots (weights, then the scale and bias
 // boxes) and the consumer warps take them in order from a shared counter.
+// How a unit's weights travel:
+constexpr int kUnitPieces = 0;  // one bulk copy per row; scale/bias boxes per row (1-D maps)
+constexpr int kUnitRows = 1;    // whole rows: the 4 rows are contiguous, one bulk copy
+constexpr int kUnitTiles = 2;   // one 2-D box of 4 rows x pitch bytes; one 2-D scale and one bias box
 struct RingParams : Params {
     int uc;                   // chunks per unit
-    int full_rows;            // 1: a unit is whole rows, loaded as one contiguous copy
+    int unit_mode;            // kUnitPieces, kUnitRows or kUnitTiles
     int pitch;                // bytes per unit row in a slot
     int sb_mode_unit;         // 1: one scale box and one bias box per unit; 0: one of each per row
-    int sbox;                 // elements per scale / bias box (a multiple of 8)
+    int sbox;                 // elements per scale / bias box (a multiple of 8; tiles: 4 rows of uc chunks' groups)
     int slots;                // ring slots (a multiple of the producer warps)
     int consumers;            // consumer warps; warps consumers.. are producers
 };
@@ -89,11 +93,13 @@ __host__ __device__ inline SmemLayout smem_layout(int bits, int V, int warps, in
 }
 
 // Shared memory of the one-vector kernel, as byte offsets from a 128-aligned
-// base: the ring, staged x, chunk values, the slot barriers and counters.
+// base: the ring, staged x'' (128 bytes a subgroup, where the raw x lands
+// first) and its (sx, f1, f2, 0), chunk values, the slot barriers and the x
+// barrier, counters.
 constexpr int kBoxAlign = 128;  // shared-memory alignment of a tensor-map box
 struct RingLayout {
     int slot_bytes, sb_off, sbs;  // slot size, offset of the scale/bias boxes in a slot, bytes per box
-    int ring, xs, cv, bar, misc, total;
+    int ring, xs, xm, cv, bar, misc, total;
 };
 
 __host__ __device__ inline RingLayout ring_layout(int pitch, int sb_mode_unit, int sbox, int slots, int nsub, int max_rb,
@@ -105,9 +111,10 @@ __host__ __device__ inline RingLayout ring_layout(int pitch, int sb_mode_unit, i
     L.slot_bytes = L.sb_off + (sb_mode_unit ? 2 : 2 * kRows) * L.sbs;
     L.ring = 0;
     L.xs = slots * L.slot_bytes;
-    L.cv = align_up(L.xs + nsub * kXsB16, 16);
+    L.xm = L.xs + nsub * 128;
+    L.cv = align_up(L.xm + nsub * 16, 16);
     L.bar = align_up(L.cv + max_rb * kRows * cpc * 4, 16);
-    L.misc = L.bar + 2 * slots * 8;
+    L.misc = L.bar + (2 * slots + 1) * 8;
     L.total = L.misc + 32 + kBoxAlign;  // next-unit counter, abort flag, issued counts; alignment slack
     return L;
 }
