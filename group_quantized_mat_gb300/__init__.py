@@ -21,7 +21,8 @@ import numpy as np
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libqmv.so")
 
-QMV_MAX_M = 16
+QMV_TILE_M = 16
+QMV_MAX_M = 256
 F32_OUT = 0x1
 FORCE_M1_PER_COLUMN = 0x2
 PDL = 0x4

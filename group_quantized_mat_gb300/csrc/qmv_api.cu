@@ -375,8 +375,11 @@ qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t 
         !aligned(y, f32_out ? 4 : 2) || (workspace && !aligned(workspace, 16)))
         return QMV_ERR_ALIGN;
 
-    const bool per_column = (flags & QMV_FORCE_M1_PER_COLUMN) != 0;
-    const int V = per_column ? 1 : M;
+    static_assert(qmv::kMaxM == QMV_TILE_M, "launch width");
+    // Vectors go through in launches of at most kMaxM (one each with
+    // QMV_FORCE_M1_PER_COLUMN); a column's arithmetic does not depend on
+    // which launch carries it, nor on how many vectors share that launch.
+    const int tile = (flags & QMV_FORCE_M1_PER_COLUMN) != 0 ? 1 : qmv::kMaxM;
 
     int dev = 0;
     cudaError_t ce = cudaGetDevice(&dev);
@@ -385,12 +388,17 @@ qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t 
     int sms = 0;
     st = sm_count(dev, &sms);
     if (st != QMV_OK) return st;
-    const Problem pr = plan(V, N, K, bits, gs, sms);
-    if (pr.smem > kSmemBudget) {  // only a tuning override can get here
-        snprintf(g_last_error, sizeof g_last_error, "launch plan needs %d bytes of shared memory", pr.smem);
+    // at most two launch widths: full tiles and the remainder
+    const int v_full = M < tile ? M : tile, v_rest = M > tile ? M % tile : 0;
+    const Problem pr_full = plan(v_full, N, K, bits, gs, sms);
+    const Problem pr_rest = v_rest ? plan(v_rest, N, K, bits, gs, sms) : pr_full;
+    if (pr_full.smem > kSmemBudget || pr_rest.smem > kSmemBudget) {  // only a tuning override can get here
+        snprintf(g_last_error, sizeof g_last_error, "launch plan needs %d bytes of shared memory",
+                 pr_full.smem > pr_rest.smem ? pr_full.smem : pr_rest.smem);
         return QMV_ERR_CUDA;
     }
-    const size_t need = workspace_bytes_for(pr);
+    const size_t need_full = workspace_bytes_for(pr_full), need_rest = workspace_bytes_for(pr_rest);
+    const size_t need = need_full > need_rest ? need_full : need_rest;
     if (need > 0) {
         if (workspace) {
             if (workspace_bytes < need) return QMV_ERR_WORKSPACE;
@@ -404,38 +412,45 @@ qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t 
     st = device_error_ptr(dev, &err);
     if (st != QMV_OK) return st;
 
-    qmv::RingMaps maps;
-    memset(&maps, 0, sizeof maps);
-    if (V == 1) {
-        int enc = encode_sb_map(&maps.s, scales, pr);
-        if (enc == 0) enc = encode_sb_map(&maps.b, biases, pr);
-        if (enc == 0 && pr.unit_mode == qmv::kUnitTiles) enc = encode_w_map(&maps.w, w_q, pr);
-        if (enc != 0) {
-            snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled returned %d%s", enc,
-                     enc < 0 ? " (driver entry point not found)" : "");
-            return QMV_ERR_CUDA;
-        }
-    }
-
-    qmv::Params p;
-    p.err = err;
-    p.w = reinterpret_cast<const uint8_t *>(w_q);
-    p.scales = scales;
-    p.biases = biases;
-    p.N = N; p.K = K; p.G = pr.G; p.S_row = pr.S_row; p.ks = pr.ks; p.row_bytes = pr.row_bytes;
-    p.NB = pr.NB; p.grid_rows = pr.grid_rows; p.cpc = pr.cpc; p.max_rb = pr.max_rb;
-    p.f32_out = f32_out ? 1 : 0;
-    p.counters = need ? static_cast<unsigned *>(workspace) : nullptr;
-    p.partials = need ? reinterpret_cast<float *>(static_cast<char *>(workspace) + counter_bytes(pr.NB)) : nullptr;
-
     const bool pdl = (flags & QMV_PDL) != 0;
     const size_t ysize = f32_out ? sizeof(float) : sizeof(uint16_t);
-    const int launches = per_column ? M : 1;
-    for (int m = 0; m < launches; ++m) {
-        p.x = x + size_t(m) * K;
-        p.y = static_cast<char *>(y) + size_t(m) * N * ysize;
-        ce = dispatch(pr, maps, p, pdl, stream);
-        if (ce != cudaSuccess) return cuda_fail("kernel launch", ce);
+    for (int pass = 0; pass < 2; ++pass) {
+        const Problem &pr = pass == 0 ? pr_full : pr_rest;
+        const int V = pass == 0 ? v_full : v_rest;
+        const int m_lo = pass == 0 ? 0 : M - v_rest;
+        const int m_hi = pass == 0 ? M - v_rest : M;
+        if (V == 0 || m_lo >= m_hi) continue;
+
+        qmv::RingMaps maps;
+        memset(&maps, 0, sizeof maps);
+        if (V == 1) {
+            int enc = encode_sb_map(&maps.s, scales, pr);
+            if (enc == 0) enc = encode_sb_map(&maps.b, biases, pr);
+            if (enc == 0 && pr.unit_mode == qmv::kUnitTiles) enc = encode_w_map(&maps.w, w_q, pr);
+            if (enc != 0) {
+                snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled returned %d%s", enc,
+                         enc < 0 ? " (driver entry point not found)" : "");
+                return QMV_ERR_CUDA;
+            }
+        }
+
+        qmv::Params p;
+        p.err = err;
+        p.w = reinterpret_cast<const uint8_t *>(w_q);
+        p.scales = scales;
+        p.biases = biases;
+        p.N = N; p.K = K; p.G = pr.G; p.S_row = pr.S_row; p.ks = pr.ks; p.row_bytes = pr.row_bytes;
+        p.NB = pr.NB; p.grid_rows = pr.grid_rows; p.cpc = pr.cpc; p.max_rb = pr.max_rb;
+        p.f32_out = f32_out ? 1 : 0;
+        const bool split = workspace_bytes_for(pr) > 0;
+        p.counters = split ? static_cast<unsigned *>(workspace) : nullptr;
+        p.partials = split ? reinterpret_cast<float *>(static_cast<char *>(workspace) + counter_bytes(pr.NB)) : nullptr;
+        for (int m = m_lo; m < m_hi; m += V) {
+            p.x = x + size_t(m) * K;
+            p.y = static_cast<char *>(y) + size_t(m) * N * ysize;
+            ce = dispatch(pr, maps, p, pdl, stream);
+            if (ce != cudaSuccess) return cuda_fail("kernel launch", ce);
+        }
     }
     return QMV_OK;
 }
@@ -463,7 +478,10 @@ extern "C" __attribute__((visibility("default"))) void qmv_tune_set(int slots, i
 extern "C" size_t qmv_workspace_size(int M, int N, int K, int bits, int group_size)
 {
     if (check_shape(M, N, K, bits, group_size, true) != QMV_OK) return 0;
-    return workspace_bytes_for(plan(M, N, K, bits, group_size, 0));
+    // launches of kMaxM vectors and one of the remainder (see run_impl)
+    const size_t full = workspace_bytes_for(plan(M < qmv::kMaxM ? M : qmv::kMaxM, N, K, bits, group_size, 0));
+    const size_t rest = M > qmv::kMaxM && M % qmv::kMaxM ? workspace_bytes_for(plan(M % qmv::kMaxM, N, K, bits, group_size, 0)) : 0;
+    return full > rest ? full : rest;
 }
 
 extern "C" qmv_status qmv_run(const uint32_t *w_q, const uint16_t *scales, const uint16_t *biases, const uint16_t *x,
@@ -514,7 +532,7 @@ extern "C" const char *qmv_status_string(qmv_status s)
         case QMV_ERR_BITS: return "QMV_ERR_BITS: bits must be 2 or 4";
         case QMV_ERR_GROUP: return "QMV_ERR_GROUP: group_size must be 64 or 128";
         case QMV_ERR_SHAPE: return "QMV_ERR_SHAPE: need 1 <= N <= 2^30, 1 <= K <= 2^24, K % group_size == 0";
-        case QMV_ERR_M_RANGE: return "QMV_ERR_M_RANGE: M must be in [1, 16]";
+        case QMV_ERR_M_RANGE: return "QMV_ERR_M_RANGE: M must be in [1, 256]";
         case QMV_ERR_ALIGN: return "QMV_ERR_ALIGN: w_q, x, scales, biases and workspace need 16-byte alignment, y 2 (f32 y: 4)";
         case QMV_ERR_CUDA: return "QMV_ERR_CUDA: a CUDA runtime call or kernel launch failed";
         case QMV_ERR_WORKSPACE: return "QMV_ERR_WORKSPACE: workspace smaller than qmv_workspace_size()";

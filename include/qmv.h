@@ -63,10 +63,16 @@ typedef enum qmv_status {
 /* The CUDA stream type (identical to cudaStream_t; 0 is the legacy default stream). */
 typedef struct CUstream_st *qmv_stream_t;
 
-/* Widest activation batch one call serves from a single read of the weights
- * (the speculative-verify width; above it a dense quantized mat-mat takes over,
- * issue #1289 "Scope limits"). */
-#define QMV_MAX_M 16
+/* Widest activation batch one launch serves from a single read of the weights
+ * (the speculative-verify width). */
+#define QMV_TILE_M 16
+
+/* Most vectors per call. A call with M > QMV_TILE_M runs as consecutive
+ * launches of QMV_TILE_M vectors and one of the remainder, reading the weights
+ * once per launch; every column's arithmetic is the same as at M = 1. (Above
+ * the batch limit the pages hand off to a dense quantized mat-mat, issue #1289
+ * "Scope limits"; this tiling is the order-preserving stand-in.) */
+#define QMV_MAX_M 256
 
 /* ------------------------------------------------------------------ codec */
 

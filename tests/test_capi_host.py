@@ -111,7 +111,13 @@ def test_split_plan(lib):
     assert w13 == (960 * 4 + 255) // 256 * 256 + 8 * 13 * 3840 * 4
     w16 = g.qmv_workspace_size(16, 3840, 15360, 4, 64)
     assert w16 - w13 == 8 * 3 * 3840 * 4
+    # M above 16 runs as launches of 16 vectors and one of the remainder: the
+    # widest of those decides
     assert g.qmv_workspace_size(17, 15360, 3840, 4, 64) == 0
+    assert g.qmv_workspace_size(20, 3840, 15360, 4, 64) == w16
+    assert g.qmv_workspace_size(33, 3840, 15360, 4, 64) == w16
+    assert g.qmv_workspace_size(256, 3840, 15360, 4, 64) == w16
+    assert g.qmv_workspace_size(257, 3840, 15360, 4, 64) == 0
     # sizes whose scale index would pass 2^31 are refused
     assert g.qmv_split_count(1 << 30, 1 << 13, 4, 64) == 0
 
@@ -123,7 +129,7 @@ FAKE = 1 << 20  # an aligned address that validation must reject before any use
     (dict(w_q=0), 1), (dict(y=0), 1),
     (dict(bits=3), 2), (dict(group_size=32), 3),
     (dict(K=1000), 4), (dict(N=0), 4), (dict(K=0), 4),
-    (dict(M=0), 5), (dict(M=17), 5),
+    (dict(M=0), 5), (dict(M=257), 5),
     (dict(w_q=FAKE + 8), 6), (dict(x=FAKE + 2), 6), (dict(scales=FAKE + 1), 6),
     (dict(scales=FAKE + 8), 6), (dict(biases=FAKE + 2), 6),
 ])

@@ -143,6 +143,20 @@ def test_wide_exponent_range(o, bits):
     assert np.all(np.abs(y6 - ref) <= 1e-4 * terms + 1e-6)
 
 
+@pytest.mark.parametrize("M", [17, 20, 33])
+def test_more_than_sixteen_vectors(o, M):
+    """M above 16 runs in launches of 16 and the remainder: every column still
+    equals the M = 1 result bit for bit and meets the tolerance."""
+    N, K = 700, 3840
+    inp = synth.make_inputs(N, K, M, 4, 64, seed=40 + M)
+    dp = DeviceProblem(inp)
+    y = dp.run(flags=g.F32_OUT)
+    singles = np.stack([dp.run(x=dp.x[m:m + 1].contiguous(), M=1, flags=g.F32_OUT)[0] for m in range(M)])
+    assert np.array_equal(y.view(np.uint32), singles.view(np.uint32))
+    ref, terms = oracle_rows(o, inp)
+    check_parity(dp.run(), ref, terms, f"M={M}")
+
+
 def test_position_invariance():
     inp = synth.make_inputs(3840, 3840, 13, 4, 64, seed=11)
     dp = DeviceProblem(inp)
