@@ -26,6 +26,7 @@ QMV_MAX_M = 256
 F32_OUT = 0x1
 FORCE_M1_PER_COLUMN = 0x2
 PDL = 0x4
+SB_INTERLEAVED = 0x8
 
 STATUS = {
     0: "QMV_OK", 1: "QMV_ERR_NULL", 2: "QMV_ERR_BITS", 3: "QMV_ERR_GROUP", 4: "QMV_ERR_SHAPE",
@@ -33,7 +34,7 @@ STATUS = {
     9: "QMV_ERR_VALUE", 10: "QMV_ERR_FLAGS",
 }
 
-EXPORTED = ("qmv_packed_words", "qmv_pack", "qmv_unpack", "qmv_split_count", "qmv_workspace_size",
+EXPORTED = ("qmv_packed_words", "qmv_pack", "qmv_unpack", "qmv_pack_sb", "qmv_split_count", "qmv_workspace_size",
             "qmv_run", "qmv_run_ex", "qmv_run_noalloc", "qmv_workspace_init", "qmv_device_error", "qmv_last_cuda_error",
             "qmv_status_string")
 
@@ -68,6 +69,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.qmv_pack.argtypes = [P, P, I64, I64, I]
         lib.qmv_unpack.restype = I
         lib.qmv_unpack.argtypes = [P, P, I64, I64, I]
+        lib.qmv_pack_sb.restype = I
+        lib.qmv_pack_sb.argtypes = [P, P, P, I64, I64]
         lib.qmv_split_count.restype = I
         lib.qmv_split_count.argtypes = [I, I, I, I]
         lib.qmv_workspace_size.restype = SZ
@@ -143,6 +146,18 @@ def qmv_unpack(w_q: np.ndarray, K: int, bits: int) -> np.ndarray:
     N = w_q.shape[0]
     out = np.empty((N, K), dtype=np.uint8)
     _check(load().qmv_unpack(w_q.ctypes.data, out.ctypes.data, N, K, bits), "qmv_unpack")
+    return out
+
+
+def qmv_pack_sb(scales: np.ndarray, biases: np.ndarray) -> np.ndarray:
+    """Interleave host bf16 bit patterns scales, biases [N, G] (uint16) into
+    uint32 [N, G]: scale in the low half of each word, bias in the high half."""
+    s = np.ascontiguousarray(scales, dtype=np.uint16)
+    b = np.ascontiguousarray(biases, dtype=np.uint16)
+    if s.shape != b.shape or s.ndim != 2:
+        raise QmvError(4, "qmv_pack_sb")
+    out = np.empty(s.shape, dtype=np.uint32)
+    _check(load().qmv_pack_sb(s.ctypes.data, b.ctypes.data, out.ctypes.data, s.shape[0], s.shape[1]), "qmv_pack_sb")
     return out
 
 

@@ -68,6 +68,7 @@ struct Problem {
     int smem;       // dynamic shared memory per CTA
     // one-vector ring
     int uc, unit_mode, pitch, sb_mode_unit, sbox, slots, consumers;
+    int sb_packed;
 };
 
 // Largest dynamic shared memory a CTA may use (static shared memory and
@@ -146,7 +147,7 @@ Problem plan_direct(int V, int N, int K, int bits, int gs, int sms)
 // are 16-byte multiples, else one copy per row), scale/bias boxes, then as
 // many ring slots as fit (a multiple of the producer warps, at most kMaxSlots
 // and the CTA's units).
-Problem plan_ring(int N, int K, int bits, int gs, int sms)
+Problem plan_ring(int N, int K, int bits, int gs, int sms, bool sb_packed)
 {
     Problem pr{};
     common_shape(pr, 1, N, K, bits, gs);
@@ -169,7 +170,7 @@ Problem plan_ring(int N, int K, int bits, int gs, int sms)
         pr.pitch = pr.row_bytes;
     } else {
         // a tile row is at most 256 eight-byte elements (kUnitMax / 4 rows)
-        pr.unit_mode = pr.G % 8 == 0 ? qmv::kUnitTiles : qmv::kUnitPieces;
+        pr.unit_mode = pr.G * qmv::sb_elem_bytes(sb_packed) % 16 == 0 ? qmv::kUnitTiles : qmv::kUnitPieces;
         pr.uc = kUnitMax / (qmv::kRows * cb);
         if (pr.uc < 1) pr.uc = 1;
         if (pr.uc > pr.cpc) pr.uc = pr.cpc;
@@ -184,19 +185,21 @@ Problem plan_ring(int N, int K, int bits, int gs, int sms)
     const int gpu = pr.unit_mode == qmv::kUnitRows
                         ? pr.G
                         : (pr.uc * qmv::kChunkElems / gs < pr.G ? pr.uc * qmv::kChunkElems / gs : pr.G);
+    pr.sb_packed = sb_packed ? 1 : 0;
+    const int A = 16 / qmv::sb_elem_bytes(pr.sb_packed);  // box start alignment, elements
     if (pr.unit_mode == qmv::kUnitTiles) {
         pr.sb_mode_unit = 1;
         pr.sbox = qmv::kRows * (pr.uc * qmv::kChunkElems / gs);  // 4 box rows, each the unit's groups
-    } else if (pr.unit_mode == qmv::kUnitRows && qmv::kRows * pr.G + 7 <= 256) {
+    } else if (pr.unit_mode == qmv::kUnitRows && qmv::kRows * pr.G + A - 1 <= 256) {
         pr.sb_mode_unit = 1;
-        pr.sbox = qmv::align_up(qmv::kRows * pr.G + 7, 8);
+        pr.sbox = qmv::align_up(qmv::kRows * pr.G + A - 1, A);
     } else {
         pr.sb_mode_unit = 0;
-        pr.sbox = qmv::align_up(gpu + 7, 8);
+        pr.sbox = qmv::align_up(gpu + A - 1, A);
     }
     const int nsub = pr.cpc * qmv::kChunkSubs < pr.S_row ? pr.cpc * qmv::kChunkSubs : pr.S_row;
     auto layout = [&](int slots) {
-        return qmv::ring_layout(pr.pitch, pr.sb_mode_unit, pr.sbox, slots, nsub, pr.max_rb, pr.cpc);
+        return qmv::ring_layout(pr.pitch, pr.sb_mode_unit, pr.sbox, pr.sb_packed, slots, nsub, pr.max_rb, pr.cpc);
     };
     const int upr = (pr.cpc + pr.uc - 1) / pr.uc;
     const int units = pr.max_rb * upr;
@@ -214,9 +217,9 @@ Problem plan_ring(int N, int K, int bits, int gs, int sms)
     return pr;
 }
 
-Problem plan(int V, int N, int K, int bits, int gs, int sms)
+Problem plan(int V, int N, int K, int bits, int gs, int sms, bool sb_packed = false)
 {
-    return V == 1 ? plan_ring(N, K, bits, gs, sms) : plan_direct(V, N, K, bits, gs, sms);
+    return V == 1 ? plan_ring(N, K, bits, gs, sms, sb_packed) : plan_direct(V, N, K, bits, gs, sms);
 }
 
 size_t counter_bytes(int NB) { return (size_t(NB) * sizeof(unsigned) + 255) & ~size_t(255); }
@@ -242,20 +245,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// Scales or biases: for tiles a 2-D bf16 tensor [N][G] whose box is 4 rows
-// of sbox / 4 groups, else a 1-D tensor of N*G elements whose box is `sbox`
-// elements. Elements outside the tensor arrive as zeros.
+// Scales or biases (or the interleaved pairs, 4-byte elements): for tiles a
+// 2-D tensor [N][G] whose box is 4 rows of sbox / 4 groups, else a 1-D tensor
+// of N*G elements whose box is `sbox` elements. Elements outside the tensor
+// arrive as zeros.
 int encode_sb_map(CUtensorMap *map, const uint16_t *base, const Problem &pr)
 {
     auto fn = encode_fn();
     if (!fn) return -1;
     CUresult r;
+    const auto dtype = pr.sb_packed ? CU_TENSOR_MAP_DATA_TYPE_UINT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
     if (pr.unit_mode == qmv::kUnitTiles) {
         const cuuint64_t dims[2] = {cuuint64_t(pr.G), cuuint64_t(pr.N)};
-        const cuuint64_t strides[1] = {cuuint64_t(pr.G) * 2};  // a multiple of 16 bytes (G % 8 == 0)
+        // a multiple of 16 bytes (the planner's condition for tiles)
+        const cuuint64_t strides[1] = {cuuint64_t(pr.G) * cuuint64_t(qmv::sb_elem_bytes(pr.sb_packed))};
         const cuuint32_t box[2] = {cuuint32_t(pr.sbox / qmv::kRows), cuuint32_t(qmv::kRows)};
         const cuuint32_t estr[2] = {1, 1};
-        r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t *>(base), dims, strides, box, estr,
+        r = fn(map, dtype, 2, const_cast<uint16_t *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     } else {
@@ -263,7 +269,7 @@ int encode_sb_map(CUtensorMap *map, const uint16_t *base, const Problem &pr)
         const cuuint64_t strides[1] = {0};
         const cuuint32_t box[1] = {cuuint32_t(pr.sbox)};
         const cuuint32_t estr[1] = {1};
-        r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 1, const_cast<uint16_t *>(base), dims, strides, box, estr,
+        r = fn(map, dtype, 1, const_cast<uint16_t *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
@@ -366,12 +372,13 @@ qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t 
                     int M, int N, int K, int bits, int gs, void *workspace, size_t workspace_bytes, unsigned flags,
                     cudaStream_t stream)
 {
-    if (!w_q || !scales || !biases || !x || !y) return QMV_ERR_NULL;
+    const bool sb_packed = (flags & QMV_SB_INTERLEAVED) != 0;
+    if (!w_q || !scales || (!biases && !sb_packed) || !x || !y) return QMV_ERR_NULL;
     qmv_status st = check_shape(M, N, K, bits, gs, true);
     if (st != QMV_OK) return st;
-    if (flags & ~(QMV_F32_OUT | QMV_FORCE_M1_PER_COLUMN | QMV_PDL)) return QMV_ERR_FLAGS;
+    if (flags & ~(QMV_F32_OUT | QMV_FORCE_M1_PER_COLUMN | QMV_PDL | QMV_SB_INTERLEAVED)) return QMV_ERR_FLAGS;
     const bool f32_out = (flags & QMV_F32_OUT) != 0;
-    if (!aligned(w_q, 16) || !aligned(x, 16) || !aligned(scales, 16) || !aligned(biases, 16) ||
+    if (!aligned(w_q, 16) || !aligned(x, 16) || !aligned(scales, 16) || (!sb_packed && !aligned(biases, 16)) ||
         !aligned(y, f32_out ? 4 : 2) || (workspace && !aligned(workspace, 16)))
         return QMV_ERR_ALIGN;
 
@@ -390,8 +397,8 @@ qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t 
     if (st != QMV_OK) return st;
     // at most two launch widths: full tiles and the remainder
     const int v_full = M < tile ? M : tile, v_rest = M > tile ? M % tile : 0;
-    const Problem pr_full = plan(v_full, N, K, bits, gs, sms);
-    const Problem pr_rest = v_rest ? plan(v_rest, N, K, bits, gs, sms) : pr_full;
+    const Problem pr_full = plan(v_full, N, K, bits, gs, sms, sb_packed);
+    const Problem pr_rest = v_rest ? plan(v_rest, N, K, bits, gs, sms, sb_packed) : pr_full;
     if (pr_full.smem > kSmemBudget || pr_rest.smem > kSmemBudget) {  // only a tuning override can get here
         snprintf(g_last_error, sizeof g_last_error, "launch plan needs %d bytes of shared memory",
                  pr_full.smem > pr_rest.smem ? pr_full.smem : pr_rest.smem);
@@ -425,7 +432,7 @@ qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t 
         memset(&maps, 0, sizeof maps);
         if (V == 1) {
             int enc = encode_sb_map(&maps.s, scales, pr);
-            if (enc == 0) enc = encode_sb_map(&maps.b, biases, pr);
+            if (enc == 0 && !sb_packed) enc = encode_sb_map(&maps.b, biases, pr);
             if (enc == 0 && pr.unit_mode == qmv::kUnitTiles) enc = encode_w_map(&maps.w, w_q, pr);
             if (enc != 0) {
                 snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled returned %d%s", enc,
@@ -442,6 +449,7 @@ qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t 
         p.N = N; p.K = K; p.G = pr.G; p.S_row = pr.S_row; p.ks = pr.ks; p.row_bytes = pr.row_bytes;
         p.NB = pr.NB; p.grid_rows = pr.grid_rows; p.cpc = pr.cpc; p.max_rb = pr.max_rb;
         p.f32_out = f32_out ? 1 : 0;
+        p.sb_packed = sb_packed ? 1 : 0;
         const bool split = workspace_bytes_for(pr) > 0;
         p.counters = split ? static_cast<unsigned *>(workspace) : nullptr;
         p.partials = split ? reinterpret_cast<float *>(static_cast<char *>(workspace) + counter_bytes(pr.NB)) : nullptr;

@@ -48,6 +48,15 @@ extern "C" qmv_status qmv_pack(const uint8_t *q, uint32_t *w_q, int64_t N, int64
     return QMV_OK;
 }
 
+extern "C" qmv_status qmv_pack_sb(const uint16_t *scales, const uint16_t *biases, uint32_t *sb, int64_t N, int64_t G)
+{
+    if (!scales || !biases || !sb) return QMV_ERR_NULL;
+    if (N < 1 || G < 1 || N > (int64_t(1) << 40) / G) return QMV_ERR_SHAPE;
+    const int64_t n = N * G;
+    for (int64_t i = 0; i < n; ++i) sb[i] = uint32_t(scales[i]) | (uint32_t(biases[i]) << 16);
+    return QMV_OK;
+}
+
 extern "C" qmv_status qmv_unpack(const uint32_t *w_q, uint8_t *q, int64_t N, int64_t K, int bits)
 {
     if (!q || !w_q) return QMV_ERR_NULL;

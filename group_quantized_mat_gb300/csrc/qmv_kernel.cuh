@@ -247,6 +247,13 @@ __device__ __forceinline__ float4 lds_f4(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ uint32_t lds_u16(uint32_t addr)
 {
     uint16_t v;
@@ -740,7 +747,7 @@ __device__ __forceinline__ void fold_chunks(const float *cvs, int nrows, int row
 
 // ------------------------------------------------------- one vector: ring --
 
-template <int BITS, int GS>
+template <int BITS, int GS, bool SBP>
 __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CUtensorMap *map_s, const CUtensorMap *map_b,
                                               const RingParams &p)
 {
@@ -769,7 +776,10 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CU
     const int nunits = (rb_hi - rb_lo) * upr;
 
     const int nsub_max = p.cpc * kChunkSubs < p.S_row ? p.cpc * kChunkSubs : p.S_row;
-    const RingLayout L = ring_layout(p.pitch, p.sb_mode_unit, p.sbox, p.slots, nsub_max, p.max_rb, p.cpc);
+    const RingLayout L = ring_layout(p.pitch, p.sb_mode_unit, p.sbox, SBP, p.slots, nsub_max, p.max_rb, p.cpc);
+    // metadata: bytes per element (a bf16, or an interleaved scale|bias pair)
+    // and the box start alignment in elements (16 bytes)
+    constexpr int sbE = sb_elem_bytes(SBP), sbA = 16 / sbE;
     const uint32_t ring = smem_u32(smem + L.ring);
     const uint32_t xs = smem_u32(smem + L.xs), xm = smem_u32(smem + L.xm);
     float *cvs = reinterpret_cast<float *>(smem + L.cv);
@@ -793,10 +803,10 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CU
         g.c1 = g.c0 + p.uc < c_hi ? g.c0 + p.uc : c_hi;
         return g;
     };
-    // Element coordinate of scale/bias box `bx` of a unit (rows r0.., groups from chunk c0).
+    // Element coordinate of metadata box `bx` of a unit (rows r0.., groups from chunk c0).
     auto sb_coord = [&](const Unit &g, int bx) {
         const long long g0 = (long long)g.c0 * kChunkElems / GS;
-        return int(((long long)(g.r0 + bx) * p.G + g0) & ~7ll);
+        return int(((long long)(g.r0 + bx) * p.G + g0) & ~(long long)(sbA - 1));
     };
 
     const uint64_t pol = l2_evict_first_policy();
@@ -808,15 +818,15 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CU
         const uint32_t seg = uint32_t(e1 - e0) * BITS / 8;
         if (p.unit_mode == kUnitTiles) {
             // boxes of 4 rows: rows past N and bytes past the row's end arrive as zeros
-            mbar_arrive_expect_tx(full, uint32_t(kRows * p.pitch + 2 * p.sbox * 2));
+            mbar_arrive_expect_tx(full, uint32_t(kRows * p.pitch + (SBP ? 1 : 2) * p.sbox * sbE));
             tma_load_2d_hint(base, map_w, g.c0 * (kChunkB / 8), g.r0, full, pol);
             tma_load_2d(base + L.sb_off, map_s, g.c0 * (kChunkElems / GS), g.r0, full);
-            tma_load_2d(base + L.sb_off + L.sbs, map_b, g.c0 * (kChunkElems / GS), g.r0, full);
+            if constexpr (!SBP) tma_load_2d(base + L.sb_off + L.sbs, map_b, g.c0 * (kChunkElems / GS), g.r0, full);
             return;
         }
         const int nbox = p.sb_mode_unit ? 1 : g.nr;
         const uint32_t wbytes = p.unit_mode == kUnitRows ? uint32_t(g.nr) * uint32_t(p.row_bytes) : uint32_t(g.nr) * seg;
-        mbar_arrive_expect_tx(full, wbytes + uint32_t(2 * nbox * p.sbox * 2));
+        mbar_arrive_expect_tx(full, wbytes + uint32_t((SBP ? 1 : 2) * nbox * p.sbox * sbE));
         if (p.unit_mode == kUnitRows) {
             bulk_load(base, p.w + size_t(g.r0) * p.row_bytes, wbytes, full, pol);
         } else {
@@ -827,7 +837,7 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CU
         for (int bx = 0; bx < nbox; ++bx) {
             const int xc = sb_coord(g, bx);
             tma_load_1d(base + L.sb_off + bx * L.sbs, map_s, xc, full);
-            tma_load_1d(base + L.sb_off + (nbox + bx) * L.sbs, map_b, xc, full);
+            if constexpr (!SBP) tma_load_1d(base + L.sb_off + (nbox + bx) * L.sbs, map_b, xc, full);
         }
     };
 
@@ -933,15 +943,15 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CU
             const Unit g = unit_geo(u);
             const uint32_t base = ring + slot * L.slot_bytes;
             const int nbox = p.sb_mode_unit ? 1 : g.nr;
-            // Per-unit shared addresses of row r's scale / bias of group 0 of
-            // the row (rows past N alias row 0).
+            // Per-unit shared addresses of row r's scale / bias (or pair) of
+            // group 0 of the row (rows past N alias row 0).
             uint32_t sa[kRows], ba[kRows];
             if (p.unit_mode == kUnitTiles) {
                 // box rows of sbox / 4 groups starting at the unit's first group
                 const int gb = p.sbox / kRows, g0 = g.c0 * (kChunkElems / GS);
 #pragma unroll
                 for (int r = 0; r < kRows; ++r) {
-                    sa[r] = base + L.sb_off + uint32_t(2 * (r * gb - g0));
+                    sa[r] = base + L.sb_off + uint32_t(sbE * (r * gb - g0));
                     ba[r] = sa[r] + L.sbs;
                 }
             } else {
@@ -950,8 +960,8 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CU
                 for (int r = 0; r < kRows; ++r) {
                     const int rr = r < g.nr ? r : 0;
                     const int bx = p.sb_mode_unit ? 0 : rr;
-                    const int xst = int(((long long)(g.r0 + bx) * p.G + g0) & ~7ll);
-                    sa[r] = base + L.sb_off + bx * L.sbs + 2 * ((g.r0 + rr) * p.G - xst);
+                    const int xst = int(((long long)(g.r0 + bx) * p.G + g0) & ~(long long)(sbA - 1));
+                    sa[r] = base + L.sb_off + bx * L.sbs + sbE * ((g.r0 + rr) * p.G - xst);
                     ba[r] = sa[r] + nbox * L.sbs;
                 }
             }
@@ -967,12 +977,19 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CU
 #pragma unroll
                     for (int pc = 0; pc < NP; ++pc)
                         quads[r][pc] = lds_v4_u32(base + uint32_t(r * p.pitch) + coff + poff[pc]);
-                const uint32_t gi2 = uint32_t(tl * (kSub / 32) / (GS / 32)) * 2;
+                // byte offset of the lane's group in a row's metadata
+                const uint32_t go = uint32_t(tl * (kSub / 32) / (GS / 32)) * uint32_t(sbE);
                 float fs[kRows], fb[kRows];
 #pragma unroll
                 for (int r = 0; r < kRows; ++r) {
-                    fs[r] = bf16_bits_to_f32(lds_u16(sa[r] + gi2));
-                    fb[r] = bf16_bits_to_f32(lds_u16(ba[r] + gi2));
+                    if constexpr (SBP) {  // one pair: scale in the low half, bias in the high half
+                        const uint32_t v = lds_u32(sa[r] + go);
+                        fs[r] = __uint_as_float(v << 16);
+                        fb[r] = __uint_as_float(v & 0xFFFF0000u);
+                    } else {
+                        fs[r] = bf16_bits_to_f32(lds_u16(sa[r] + go));
+                        fb[r] = bf16_bits_to_f32(lds_u16(ba[r] + go));
+                    }
                 }
                 const uint32_t sl = uint32_t(tl - sub_lo);
                 const float tot = chunk_v1<BITS>(quads, xs + sl * 128u, sl & 7u, xm + sl * 16u, fs, fb, active, lane);
@@ -1002,7 +1019,7 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CU
 
 // ------------------------------------------------ V vectors: direct loads --
 
-template <int BITS, int GS, int V>
+template <int BITS, int GS, int V, bool SBP>
 __device__ __forceinline__ void qmv_direct_body(const Params &p)
 {
     using T = Traits<BITS, V>;
@@ -1069,8 +1086,14 @@ __device__ __forceinline__ void qmv_direct_body(const Params &p)
             for (int pc = 0; pc < T::NP; ++pc)
                 wq[r][pc] = __ldg(reinterpret_cast<const uint4 *>(src + (BITS == 4 ? (poff[pc] & 31u) : 0u)));
             const size_t e = size_t(row) * p.G + gi;
-            sv[r] = __ldg(p.scales + e);
-            bv[r] = __ldg(p.biases + e);
+            if constexpr (SBP) {  // one pair: scale in the low half, bias in the high half
+                const uint32_t v = __ldg(reinterpret_cast<const uint32_t *>(p.scales) + e);
+                sv[r] = v & 0xFFFFu;
+                bv[r] = v >> 16;
+            } else {
+                sv[r] = __ldg(p.scales + e);
+                bv[r] = __ldg(p.biases + e);
+            }
         }
     };
 
@@ -1153,18 +1176,19 @@ constexpr int kProducersV1 = 4;
 constexpr int kThreadsV1 = (kConsumersV1 + kProducersV1) * 32;
 constexpr int kThreadsVN = 12 * 32;
 
-template <int BITS, int GS>
+// SBP: scales and biases arrive interleaved (one 32-bit pair per group).
+template <int BITS, int GS, bool SBP>
 __global__ void __launch_bounds__(kThreadsV1, 1)
     qmv_m1(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_s,
            const __grid_constant__ CUtensorMap map_b, const RingParams p)
 {
-    qmv_ring_body<BITS, GS>(&map_w, &map_s, &map_b, p);
+    qmv_ring_body<BITS, GS, SBP>(&map_w, &map_s, &map_b, p);
 }
 
-template <int BITS, int GS, int V>
+template <int BITS, int GS, int V, bool SBP>
 __global__ void __launch_bounds__(kThreadsVN, 1) qmv_streamed(const Params p)
 {
-    qmv_direct_body<BITS, GS, V>(p);
+    qmv_direct_body<BITS, GS, V, SBP>(p);
 }
 
 }  // namespace qmv

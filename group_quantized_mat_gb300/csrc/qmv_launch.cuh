@@ -43,15 +43,17 @@ cudaError_t launch_one(Kern kern, int (&configured)[64], const Launch &l, cudaSt
 template <int BITS, int GS>
 cudaError_t launch_m1(const RingMaps &maps, const RingParams &p, const Launch &l, cudaStream_t stream)
 {
-    static int configured[64] = {0};
-    return launch_one(qmv_m1<BITS, GS>, configured, l, stream, maps.w, maps.s, maps.b, p);
+    static int configured[2][64] = {};
+    if (p.sb_packed) return launch_one(qmv_m1<BITS, GS, true>, configured[1], l, stream, maps.w, maps.s, maps.b, p);
+    return launch_one(qmv_m1<BITS, GS, false>, configured[0], l, stream, maps.w, maps.s, maps.b, p);
 }
 
 template <int BITS, int GS, int V>
 cudaError_t launch_v(const Params &p, const Launch &l, cudaStream_t stream)
 {
-    static int configured[64] = {0};
-    return launch_one(qmv_streamed<BITS, GS, V>, configured, l, stream, p);
+    static int configured[2][64] = {};
+    if (p.sb_packed) return launch_one(qmv_streamed<BITS, GS, V, true>, configured[1], l, stream, p);
+    return launch_one(qmv_streamed<BITS, GS, V, false>, configured[0], l, stream, p);
 }
 
 template <int BITS, int GS>

@@ -49,6 +49,7 @@ struct Params {
     int cpc;                  // chunks per CTA
     int max_rb;               // row blocks of the largest CTA share
     int f32_out;
+    int sb_packed;            // 1: scales is the interleaved uint32 array (scale low, bias high), biases unused
 };
 
 // The one-vector kernel's ring: units are (row block, piece) pairs, a piece
@@ -64,7 +65,7 @@ struct RingParams : Params {
     int unit_mode;            // kUnitPieces, kUnitRows or kUnitTiles
     int pitch;                // bytes per unit row in a slot
     int sb_mode_unit;         // 1: one scale box and one bias box per unit; 0: one of each per row
-    int sbox;                 // elements per scale / bias box (a multiple of 8; tiles: 4 rows of uc chunks' groups)
+    int sbox;                 // elements per metadata box (a multiple of 16 bytes; tiles: 4 rows of uc chunks' groups)
     int slots;                // ring slots (a multiple of the producer warps)
     int consumers;            // consumer warps; warps consumers.. are producers
 };
@@ -102,13 +103,17 @@ struct RingLayout {
     int ring, xs, xm, cv, bar, misc, total;
 };
 
-__host__ __device__ inline RingLayout ring_layout(int pitch, int sb_mode_unit, int sbox, int slots, int nsub, int max_rb,
-                                                  int cpc)
+// Metadata element bytes: a bf16 scale or bias, or an interleaved pair.
+__host__ __device__ constexpr int sb_elem_bytes(int sb_packed) { return sb_packed ? 4 : 2; }
+
+__host__ __device__ inline RingLayout ring_layout(int pitch, int sb_mode_unit, int sbox, int sb_packed, int slots,
+                                                  int nsub, int max_rb, int cpc)
 {
     RingLayout L;
-    L.sbs = align_up(sbox * 2, kBoxAlign);
+    L.sbs = align_up(sbox * sb_elem_bytes(sb_packed), kBoxAlign);
     L.sb_off = align_up(kRows * pitch, kBoxAlign);
-    L.slot_bytes = L.sb_off + (sb_mode_unit ? 2 : 2 * kRows) * L.sbs;
+    // boxes per slot: one per unit or one per row, of each metadata tensor
+    L.slot_bytes = L.sb_off + (sb_mode_unit ? 1 : kRows) * (sb_packed ? 1 : 2) * L.sbs;
     L.ring = 0;
     L.xs = slots * L.slot_bytes;
     L.xm = L.xs + nsub * 128;

@@ -93,6 +93,16 @@ QMV_API qmv_status qmv_pack(const uint8_t *q, uint32_t *w_q, int64_t N, int64_t 
 /* Inverse of qmv_pack (host to host). Same errors except QMV_ERR_VALUE. */
 QMV_API qmv_status qmv_unpack(const uint32_t *w_q, uint8_t *q, int64_t N, int64_t K, int bits);
 
+/* Interleaves the per-group metadata into one word per group (host to host):
+ * sb[i] = scales[i] | (biases[i] << 16) for i < N*G, scales and biases being
+ * bf16 bit patterns [N, G], sb uint32 [N, G] (caller-allocated). A call with
+ * QMV_SB_INTERLEAVED reads this array through its `scales` argument: one load
+ * (or one tensor-map box) brings both values of a group where the separate
+ * arrays need two (PR #1681 "What is here as an instrument" prices the scale
+ * and bias loads). The arithmetic, and so every result, is unchanged.
+ * Errors: QMV_ERR_NULL, QMV_ERR_SHAPE (N < 1, G < 1 or N*G >= 2^40). */
+QMV_API qmv_status qmv_pack_sb(const uint16_t *scales, const uint16_t *biases, uint32_t *sb, int64_t N, int64_t G);
+
 /* ------------------------------------------------------------------- plan */
 
 /* Number of K-chunks (2048 elements each, the last one possibly shorter) that
@@ -150,6 +160,9 @@ QMV_API qmv_status qmv_run(const uint32_t *w_q, const uint16_t *scales, const ui
  * when the preceding kernel does not write w_q, scales or biases -- the
  * decode-loop case, where weights are constant. */
 #define QMV_PDL 0x4u
+/* `scales` is the uint32 [N, K/group_size] array of qmv_pack_sb (16-byte
+ * aligned); `biases` is not read and may be NULL. */
+#define QMV_SB_INTERLEAVED 0x8u
 
 /* qmv_run with an explicit workspace and flags.
  *

@@ -144,10 +144,33 @@ def test_run_validation_before_gpu(lib, kw, code):
 def test_run_ex_rejects_flags(lib):
     r = lib.qmv_run_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 64, 1024, 4, 64, None, 0, 0x100, None)
     assert r == 10
-    r = lib.qmv_run_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 64, 1024, 4, 64, None, 0, 0x8, None)
+    r = lib.qmv_run_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 64, 1024, 4, 64, None, 0, 0x10, None)
     assert r == 10
     r = lib.qmv_run_ex(FAKE, FAKE, FAKE, FAKE, FAKE + 2, 1, 64, 1024, 4, 64, None, 0, g.F32_OUT, None)
     assert r == 6
+
+
+def test_run_ex_interleaved_metadata_validation(lib):
+    # with QMV_SB_INTERLEAVED the biases pointer is not read (NULL allowed) ...
+    r = lib.qmv_run_ex(FAKE, FAKE + 8, None, FAKE, FAKE, 1, 64, 1024, 4, 64, None, 0, g.SB_INTERLEAVED, None)
+    assert r == 6  # ... and the interleaved array must be 16-byte aligned
+    r = lib.qmv_run_ex(FAKE, None, None, FAKE, FAKE, 1, 64, 1024, 4, 64, None, 0, g.SB_INTERLEAVED, None)
+    assert r == 1
+    r = lib.qmv_run_ex(FAKE, FAKE, None, FAKE, FAKE, 1, 64, 1024, 4, 64, None, 0, 0, None)
+    assert r == 1  # without the flag the biases are required
+
+
+def test_pack_sb_interleaves_scale_low_bias_high(lib):
+    rng = np.random.default_rng(3)
+    s = rng.integers(0, 1 << 16, size=(5, 7), dtype=np.uint16)
+    b = rng.integers(0, 1 << 16, size=(5, 7), dtype=np.uint16)
+    sb = g.qmv_pack_sb(s, b)
+    assert sb.dtype == np.uint32 and sb.shape == (5, 7)
+    assert np.array_equal(sb & 0xFFFF, s) and np.array_equal(sb >> 16, b)
+    out = np.empty(4, dtype=np.uint32)
+    assert lib.qmv_pack_sb(None, b.ctypes.data, out.ctypes.data, 1, 4) == 1
+    assert lib.qmv_pack_sb(s.ctypes.data, b.ctypes.data, out.ctypes.data, 0, 4) == 4
+    assert lib.qmv_pack_sb(s.ctypes.data, b.ctypes.data, out.ctypes.data, 4, 0) == 4
 
 
 def test_status_strings(lib):

@@ -157,6 +157,28 @@ def test_more_than_sixteen_vectors(o, M):
     check_parity(dp.run(), ref, terms, f"M={M}")
 
 
+@pytest.mark.parametrize("N,K,bits,gs", [
+    (15360, 3840, 4, 64),   # whole-row units, one metadata box per unit
+    (3840, 15360, 4, 64),   # 2-D tile units
+    (100, 4160, 4, 64),     # per-row pieces (G = 65)
+    (300, 3840, 2, 128),
+    (70, 11264, 4, 128),    # G = 88: tiles
+])
+def test_interleaved_metadata_gives_identical_results(N, K, bits, gs):
+    """QMV_SB_INTERLEAVED changes how scales and biases travel, not the
+    arithmetic: the results equal the separate layout's bit for bit."""
+    inp = synth.make_inputs(N, K, 13, bits, gs, seed=60 + K)
+    dp = DeviceProblem(inp)
+    sb = dev(g.qmv_pack_sb(inp.scales, inp.biases))
+    for M in (1, 4, 13):
+        x = dp.x[:M].contiguous()
+        want = dp.run(x=x, M=M, flags=g.F32_OUT)
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        g.qmv_run_ex(dp.w, sb, None, x, y, M, N, K, bits, gs, flags=g.F32_OUT | g.SB_INTERLEAVED)
+        torch.cuda.synchronize()
+        assert np.array_equal(y.cpu().numpy().view(np.uint32), want.view(np.uint32)), f"M={M}"
+
+
 def test_position_invariance():
     inp = synth.make_inputs(3840, 3840, 13, 4, 64, seed=11)
     dp = DeviceProblem(inp)
