@@ -69,6 +69,7 @@ struct Problem {
     // one-vector ring
     int uc, unit_mode, pitch, sb_mode_unit, sbox, slots, consumers;
     int sb_packed;
+    int xf32;       // streamed kernel: fp32 staging of x'
 };
 
 // Largest dynamic shared memory a CTA may use (static shared memory and
@@ -83,7 +84,7 @@ constexpr int kMaxSlots = 24;
 
 #if defined(QMV_TUNING)
 // Tuning builds only: fixed launch shapes for sweeps (0 = automatic).
-struct TuneOverride { int slots = 0, uc = 0, consumers = 0, grid_rows = 0, cpc = 0; };
+struct TuneOverride { int slots = 0, uc = 0, consumers = 0, grid_rows = 0, cpc = 0, xf32 = -1; };
 TuneOverride g_tune;
 #endif
 
@@ -99,13 +100,14 @@ void common_shape(Problem &pr, int V, int N, int K, int bits, int gs)
 
 // A persistent grid of about one CTA per SM: the chunk ranges times an even
 // split of the row blocks; more CTAs (several waves) when a share of rows
-// would exceed the chunk-value cap.
-void grid_shape(Problem &pr, int sms, int V)
+// would exceed what `cv_bytes` of chunk values hold.
+void grid_shape(Problem &pr, int sms, int V, int cv_bytes)
 {
     pr.nranges = (pr.ks + pr.cpc - 1) / pr.cpc;
     int gr = sms > 0 ? sms / pr.nranges : 1;
     if (gr < 1) gr = 1;
-    const int rb_cap = kCvBudget / (qmv::kRows * pr.cpc * V * 4) > 0 ? kCvBudget / (qmv::kRows * pr.cpc * V * 4) : 1;
+    const int per_rb = qmv::kRows * pr.cpc * V * 4;
+    const int rb_cap = cv_bytes / per_rb > 0 ? cv_bytes / per_rb : 1;
     if ((pr.NB + gr - 1) / gr > rb_cap) gr = (pr.NB + rb_cap - 1) / rb_cap;
     if (gr > pr.NB) gr = pr.NB;
 #if defined(QMV_TUNING)
@@ -116,7 +118,9 @@ void grid_shape(Problem &pr, int sms, int V)
 }
 
 // Streamed kernel (V >= 2): all of K per CTA (no workspace) when the staged
-// x fits, else the widest chunk range that fits (one chunk always does).
+// x fits, else the widest chunk range that fits (one chunk always does). x' is
+// staged as fp32 unless that needs a narrower range than bf16 would while
+// bf16 covers all of K (the split then costs more than the unpacking saves).
 // Whether a workspace is needed never depends on `sms` (the fit is checked
 // against the chunk-value cap), so qmv_workspace_size needs no GPU.
 Problem plan_direct(int V, int N, int K, int bits, int gs, int sms)
@@ -125,19 +129,27 @@ Problem plan_direct(int V, int N, int K, int bits, int gs, int sms)
     common_shape(pr, V, N, K, bits, gs);
     const int warps = qmv::kStreamedWarps;
     const int wbuf = qmv::vectors_per_pass(V) < V ? warps * qmv::kRows * 32 * qmv::sub_bytes(bits) : 0;
-    auto fits = [&](int cpc) {
-        const int nsub = cpc * qmv::kChunkSubs < pr.S_row ? cpc * qmv::kChunkSubs : pr.S_row;
-        return qmv::align_up(V * nsub * qmv::kXsB16, 16) + kCvBudget + wbuf + 16 + 128 <= kSmemBudget;
+    auto nsub_of = [&](int cpc) { return cpc * qmv::kChunkSubs < pr.S_row ? cpc * qmv::kChunkSubs : pr.S_row; };
+    auto xs_bytes = [&](int cpc, bool xf32) { return qmv::align_up(V * nsub_of(cpc) * qmv::xs_cell(xf32), 16); };
+    auto widest = [&](bool xf32) {
+        int cpc = pr.ks;
+        while (cpc > 1 && xs_bytes(cpc, xf32) + kCvBudget + wbuf + 16 + 128 > kSmemBudget) --cpc;
+        return cpc;
     };
-    pr.cpc = pr.ks;
-    while (pr.cpc > 1 && !fits(pr.cpc)) --pr.cpc;
+    const int cpc32 = widest(true), cpc16 = widest(false);
+    pr.xf32 = (cpc32 == pr.ks || cpc16 < pr.ks) ? 1 : 0;
+#if defined(QMV_TUNING)
+    if (g_tune.xf32 >= 0) pr.xf32 = g_tune.xf32;
+#endif
+    pr.cpc = pr.xf32 ? cpc32 : cpc16;
 #if defined(QMV_TUNING)
     if (g_tune.cpc > 0 && g_tune.cpc <= pr.ks) pr.cpc = g_tune.cpc;
 #endif
     pr.threads = 32 * warps;
-    grid_shape(pr, sms, V);
-    const int nsub = pr.cpc * qmv::kChunkSubs < pr.S_row ? pr.cpc * qmv::kChunkSubs : pr.S_row;
-    pr.smem = qmv::smem_layout(bits, V, warps, nsub, pr.max_rb, pr.cpc).total;
+    // chunk values may use whatever shared memory the staged x and the
+    // weight buffer leave (at least kCvBudget, by the fit above)
+    grid_shape(pr, sms, V, kSmemBudget - (xs_bytes(pr.cpc, pr.xf32) + wbuf + 16 + 128 + 16));
+    pr.smem = qmv::smem_layout(bits, V, warps, nsub_of(pr.cpc), pr.max_rb, pr.cpc, pr.xf32).total;
     return pr;
 }
 
@@ -158,7 +170,7 @@ Problem plan_ring(int N, int K, int bits, int gs, int sms, bool sb_packed)
     if (g_tune.cpc > 0 && g_tune.cpc <= pr.ks) pr.cpc = g_tune.cpc;
     if (g_tune.consumers > 0 && g_tune.consumers <= qmv::kRingConsumers) pr.consumers = g_tune.consumers;
 #endif
-    grid_shape(pr, sms, 1);
+    grid_shape(pr, sms, 1, kCvBudget);
     const int cb = qmv::chunk_bytes(bits);
     bool whole = pr.cpc == pr.ks && qmv::kRows * pr.row_bytes <= kUnitMax;
 #if defined(QMV_TUNING)
@@ -450,6 +462,7 @@ qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t 
         p.NB = pr.NB; p.grid_rows = pr.grid_rows; p.cpc = pr.cpc; p.max_rb = pr.max_rb;
         p.f32_out = f32_out ? 1 : 0;
         p.sb_packed = sb_packed ? 1 : 0;
+        p.xf32 = pr.xf32;
         const bool split = workspace_bytes_for(pr) > 0;
         p.counters = split ? static_cast<unsigned *>(workspace) : nullptr;
         p.partials = split ? reinterpret_cast<float *>(static_cast<char *>(workspace) + counter_bytes(pr.NB)) : nullptr;
@@ -481,6 +494,7 @@ extern "C" __attribute__((visibility("default"))) void qmv_tune_set(int slots, i
     g_tune.grid_rows = grid_rows;
     g_tune.cpc = cpc;
 }
+extern "C" __attribute__((visibility("default"))) void qmv_tune_xf32(int xf32) { g_tune.xf32 = xf32; }
 #endif
 
 extern "C" size_t qmv_workspace_size(int M, int N, int K, int bits, int group_size)

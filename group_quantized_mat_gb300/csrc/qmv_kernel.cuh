@@ -436,9 +436,10 @@ __device__ __forceinline__ void subgroup_dot_v1(const uint4 (&quads)[kRows][BITS
     }
 }
 
-// Step 1 for VP vectors from bf16-staged x': acc[r][v].
-//   xsub   shared address of vector 0's staged subgroup; xv bytes between vectors.
-template <int BITS, int VP>
+// Step 1 for VP vectors: acc[r][v].
+//   xsub   shared address of vector 0's staged subgroup (octet o at 32 * o
+//          for fp32 x', 16 * o for bf16 x'); xv bytes between vectors.
+template <int BITS, int VP, bool XF32>
 __device__ __forceinline__ void subgroup_dot_vp(const uint4 (&quads)[kRows][BITS == 4 ? 2 : 1], uint32_t xsub,
                                                 uint32_t xv, uint64_t (&acc)[kRows][VP])
 {
@@ -453,11 +454,17 @@ __device__ __forceinline__ void subgroup_dot_vp(const uint4 (&quads)[kRows][BITS
         for (int r = 0; r < kRows; ++r) subgroup_octet<BITS>(quads[r], o, q[r]);
 #pragma unroll
         for (int v = 0; v < VP; ++v) {
-            const uint4 xb = lds_v4_u32(xsub + v * xv + o * 16);
-            const uint64_t x01 = pack2(xb.x << 16, xb.x & 0xFFFF0000u);
-            const uint64_t x23 = pack2(xb.y << 16, xb.y & 0xFFFF0000u);
-            const uint64_t x45 = pack2(xb.z << 16, xb.z & 0xFFFF0000u);
-            const uint64_t x67 = pack2(xb.w << 16, xb.w & 0xFFFF0000u);
+            uint64_t x01, x23, x45, x67;
+            if constexpr (XF32) {
+                lds_v2_u64(xsub + v * xv + o * 32, x01, x23);
+                lds_v2_u64(xsub + v * xv + o * 32 + 16, x45, x67);
+            } else {
+                const uint4 xb = lds_v4_u32(xsub + v * xv + o * 16);
+                x01 = pack2(xb.x << 16, xb.x & 0xFFFF0000u);
+                x23 = pack2(xb.y << 16, xb.y & 0xFFFF0000u);
+                x45 = pack2(xb.z << 16, xb.z & 0xFFFF0000u);
+                x67 = pack2(xb.w << 16, xb.w & 0xFFFF0000u);
+            }
 #pragma unroll
             for (int r = 0; r < kRows; ++r) {
                 acc[r][v] = ffma2(q[r][0], x01, acc[r][v]);
@@ -471,7 +478,7 @@ __device__ __forceinline__ void subgroup_dot_vp(const uint4 (&quads)[kRows][BITS
 
 // subgroup_dot_vp with the weight bytes re-read from shared memory (cell
 // (r, pc) of this lane at wcell + (r*NP + pc) * 512), for two-pass V.
-template <int BITS, int VP>
+template <int BITS, int VP, bool XF32>
 __device__ __forceinline__ void subgroup_dot_vp_smem(uint32_t wcell, uint32_t xsub, uint32_t xv,
                                                      uint64_t (&acc)[kRows][VP])
 {
@@ -481,7 +488,7 @@ __device__ __forceinline__ void subgroup_dot_vp_smem(uint32_t wcell, uint32_t xs
     for (int r = 0; r < kRows; ++r)
 #pragma unroll
         for (int pc = 0; pc < NP; ++pc) quads[r][pc] = lds_v4_u32(wcell + uint32_t(r * NP + pc) * 512u);
-    subgroup_dot_vp<BITS, VP>(quads, xsub, xv, acc);
+    subgroup_dot_vp<BITS, VP, XF32>(quads, xsub, xv, acc);
 }
 
 // Step 2: the subgroup's term from its pair sums.
@@ -549,14 +556,15 @@ template <int BITS, bool BF16_FIELDS>
 __device__ __forceinline__ void stage_eight(const uint4 &raw, uint4 &packed, float4 &meta)
 {
     const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-    uint32_t e = 1;
+    uint32_t bits[8], e = 1, emin = 255;
     float xv[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const uint32_t bits = (i & 1) ? (w4[i / 2] >> 16) : (w4[i / 2] & 0xFFFFu);
-        xv[i] = bf16_bits_to_f32(bits);
-        const uint32_t f = (bits >> 7) & 0xFFu;
+        bits[i] = (i & 1) ? (w4[i / 2] >> 16) : (w4[i / 2] & 0xFFFFu);
+        xv[i] = bf16_bits_to_f32(bits[i]);
+        const uint32_t f = (bits[i] >> 7) & 0xFFu;
         e = f > e ? f : e;
+        emin = f < emin ? f : emin;
     }
     // largest exponent field of the subgroup
 #pragma unroll
@@ -565,26 +573,35 @@ __device__ __forceinline__ void stage_eight(const uint4 &raw, uint4 &packed, flo
         e = o > e ? o : e;
     }
     // x' = x * 2^(254 - bits*k - E) (k: position in the 16-bit half) or
-    // x'' = x * 2^(238 - bits*j - E) (j: position in the byte), as two
-    // exact power-of-two factors; elements more than 231 binades below
-    // E become a zero of their sign
-    float xr[8];
+    // x'' = x * 2^(238 - bits*j - E) (j: position in the byte); elements more
+    // than 231 binades below E become a zero of their sign. For a normal x
+    // within those 231 binades the scaled exponent field stays in [1, 254]
+    // (at the extreme, 238 - 6 - 231 = 1), so the product is an integer add
+    // to the exponent field; otherwise (zeros, subnormals, dropped elements)
+    // it is formed with two exact power-of-two multiplies.
+    uint32_t xr[8];
+    if (emin >= 1 && int(e) - int(emin) <= 231) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int k = BF16_FIELDS ? (BITS == 4 ? (i & 1) : (i & 3)) : (BITS == 4 ? (i & 3) : i);
-        const int pw = (BF16_FIELDS ? 238 : 254) - BITS * k - int(e);
-        const int p1 = pw < 127 ? pw : 127;
-        const float m1 = __uint_as_float(uint32_t(p1 + 127) << 23);
-        const float m2 = __uint_as_float(uint32_t(pw - p1 + 127) << 23);
-        const uint32_t xb = __float_as_uint(xv[i]);
-        xr[i] = int(e) - int((xb >> 23) & 0xFFu) > 231 ? __uint_as_float(xb & 0x80000000u)
-                                                        : bf16_round(__fmul_rn(__fmul_rn(xv[i], m1), m2));
+        for (int i = 0; i < 8; ++i) {
+            const int k = BF16_FIELDS ? (BITS == 4 ? (i & 1) : (i & 3)) : (BITS == 4 ? (i & 3) : i);
+            const int pw = (BF16_FIELDS ? 238 : 254) - BITS * k - int(e);
+            xr[i] = bits[i] + (uint32_t(pw) << 7);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int k = BF16_FIELDS ? (BITS == 4 ? (i & 1) : (i & 3)) : (BITS == 4 ? (i & 3) : i);
+            const int pw = (BF16_FIELDS ? 238 : 254) - BITS * k - int(e);
+            const int p1 = pw < 127 ? pw : 127;
+            const float m1 = __uint_as_float(uint32_t(p1 + 127) << 23);
+            const float m2 = __uint_as_float(uint32_t(pw - p1 + 127) << 23);
+            const float r = int(e) - int((bits[i] >> 7) & 0xFFu) > 231 ? __uint_as_float((bits[i] & 0x8000u) << 16)
+                                                                        : bf16_round(__fmul_rn(__fmul_rn(xv[i], m1), m2));
+            xr[i] = __float_as_uint(r) >> 16;
+        }
     }
-    uint32_t pk[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        pk[i] = (__float_as_uint(xr[2 * i]) >> 16) | (__float_as_uint(xr[2 * i + 1]) & 0xFFFF0000u);
-    packed = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    packed = make_uint4((xr[0] & 0xFFFFu) | (xr[1] << 16), (xr[2] & 0xFFFFu) | (xr[3] << 16),
+                        (xr[4] & 0xFFFFu) | (xr[5] << 16), (xr[6] & 0xFFFFu) | (xr[7] << 16));
     // eight-element sum, left to right; the subgroup's sum gathers the eight in order
     float s8 = xv[0];
 #pragma unroll
@@ -611,28 +628,44 @@ __device__ __forceinline__ int octet_position(int t, int e8)
 // Stages x of subgroups [sub_lo, sub_lo + nsub) of every vector at smem + xs_off,
 // loading it from global memory (the streamed kernel): eight threads per
 // subgroup, eight elements each; threads [0, nthreads) of the CTA take part.
-// Each subgroup is kXsB16 bytes: its 64 bf16 x' (octets in processing order),
-// then (sx, f1, f2, 0) as floats.
-template <int BITS, int V>
+// Each subgroup is xs_cell(XF32) bytes: its 64 x' (octets in processing
+// order) as fp32 (the values are exactly the bf16 x') or as bf16, then
+// (sx, f1, f2, 0). fp32 spares the datapath the unpacking of bf16 pairs, once
+// per vector and octet; bf16 takes half the shared memory.
+template <int BITS, int V, bool XF32>
 __device__ __forceinline__ void stage_x(uint8_t *smem, int xs_off, const uint16_t *x, int K, int sub_lo, int nsub,
                                         int nsub_max, int tid, int nthreads)
 {
     const int per_vec = nsub * 8, all = V * per_vec;
     const int all_pad = (all + nthreads - 1) / nthreads * nthreads;
-    for (int u = tid; u < all_pad; u += nthreads) {
-        const bool live = u < all;  // uniform over each eight-lane group
-        const int v = live ? u / per_vec : 0;
-        const int rem = live ? u - v * per_vec : 0;
-        const int sl = rem >> 3, e8 = rem & 7;  // subgroup (CTA-local), eighth
-        uint4 raw = make_uint4(0, 0, 0, 0);
-        if (live) raw = __ldg(reinterpret_cast<const uint4 *>(x + size_t(v) * K + size_t(sub_lo + sl) * kSub) + e8);
-        uint4 packed;
-        float4 meta;
-        stage_eight<BITS, false>(raw, packed, meta);
-        if (live) {
-            uint8_t *cell = smem + xs_off + (size_t(v) * nsub_max + sl) * kXsB16;
-            *reinterpret_cast<uint4 *>(cell + octet_position<BITS>(sub_lo + sl, e8) * 16) = packed;
-            if (e8 == 0) *reinterpret_cast<float4 *>(cell + 128) = meta;
+    // kB tasks of a thread at a time: their dependent chains (the exponent
+    // maximum, the scaling, the eight-lane sum) overlap
+    constexpr int kB = 4;
+    for (int u0 = tid; u0 < all_pad; u0 += kB * nthreads) {
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+            const int u = u0 + b * nthreads;
+            const bool live = u < all;  // uniform over each eight-lane group; dead tasks only shuffle
+            const int v = live ? u / per_vec : 0;
+            const int rem = live ? u - v * per_vec : 0;
+            const int sl = rem >> 3, e8 = rem & 7;  // subgroup (CTA-local), eighth
+            uint4 raw = make_uint4(0, 0, 0, 0);
+            if (live)
+                raw = __ldg(reinterpret_cast<const uint4 *>(x + size_t(v) * K + size_t(sub_lo + sl) * kSub) + e8);
+            uint4 packed;
+            float4 meta;
+            stage_eight<BITS, false>(raw, packed, meta);
+            if (live) {
+                uint8_t *cell = smem + xs_off + (size_t(v) * nsub_max + sl) * xs_cell(XF32);
+                if constexpr (XF32) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(cell + octet_position<BITS>(sub_lo + sl, e8) * 32);
+                    dst[0] = make_uint4(packed.x << 16, packed.x & 0xFFFF0000u, packed.y << 16, packed.y & 0xFFFF0000u);
+                    dst[1] = make_uint4(packed.z << 16, packed.z & 0xFFFF0000u, packed.w << 16, packed.w & 0xFFFF0000u);
+                } else {
+                    *reinterpret_cast<uint4 *>(cell + octet_position<BITS>(sub_lo + sl, e8) * 16) = packed;
+                }
+                if (e8 == 0) *reinterpret_cast<float4 *>(cell + (XF32 ? 256 : 128)) = meta;
+            }
         }
     }
 }
@@ -729,19 +762,44 @@ __device__ __forceinline__ void fold_chunks(const float *cvs, int nrows, int row
     __syncthreads();
     if (s_ticket != nranges - 1) return;
     __threadfence();
-    for (int idx = tid; idx < nrows * V; idx += nthreads) {
-        const int v = idx / nrows, r = idx - v * nrows;
-        const int n = row_t0 + r;
-        if (n >= N) continue;
-        float *pp = partials + size_t(v) * N + n;
-        float acc = __ldcg(pp);
-        __stcg(pp, 0.0f);
-        for (int c = 1; c < ks; ++c) {
-            float *pc = pp + size_t(c) * V * N;
-            acc = __fadd_rn(acc, __ldcg(pc));
-            __stcg(pc, 0.0f);
+    // The fold of every (vector, row) of the range, left to right over the
+    // ks chunk values: kU items per thread and up to kC chunks of each are
+    // loaded before they are added, so the round trips overlap.
+    constexpr int kU = 8, kC = 4;
+    const size_t plane = size_t(V) * N;
+    for (int base = tid; base < nrows * V; base += nthreads * kU) {
+        size_t off[kU];
+        bool ok[kU];
+        float acc[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int idx = base + u * nthreads;
+            const int v = idx / nrows, r = idx - v * nrows;
+            ok[u] = idx < nrows * V && row_t0 + r < N;
+            off[u] = ok[u] ? size_t(v) * N + size_t(row_t0 + r) : 0;
+            acc[u] = 0.0f;
         }
-        store_y(v, n, acc);
+        for (int c0 = 0; c0 < ks; c0 += kC) {
+            float t[kC][kU];
+#pragma unroll
+            for (int c = 0; c < kC; ++c)
+#pragma unroll
+                for (int u = 0; u < kU; ++u)
+                    t[c][u] = ok[u] && c0 + c < ks ? __ldcg(partials + size_t(c0 + c) * plane + off[u]) : 0.0f;
+#pragma unroll
+            for (int c = 0; c < kC; ++c)
+#pragma unroll
+                for (int u = 0; u < kU; ++u)
+                    if (c0 + c < ks) acc[u] = c0 + c == 0 ? t[c][u] : __fadd_rn(acc[u], t[c][u]);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            if (!ok[u]) continue;
+            const int idx = base + u * nthreads;
+            const int v = idx / nrows;
+            store_y(v, int(off[u] - size_t(v) * N), acc[u]);
+            for (int c = 0; c < ks; ++c) __stcg(partials + size_t(c) * plane + off[u], 0.0f);  // zero again
+        }
     }
 }
 
@@ -1019,7 +1077,7 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CU
 
 // ------------------------------------------------ V vectors: direct loads --
 
-template <int BITS, int GS, int V, bool SBP>
+template <int BITS, int GS, int V, bool SBP, bool XF32>
 __device__ __forceinline__ void qmv_direct_body(const Params &p)
 {
     using T = Traits<BITS, V>;
@@ -1043,7 +1101,7 @@ __device__ __forceinline__ void qmv_direct_body(const Params &p)
     const int nunits = (rb_hi - rb_lo) * cpc_here;  // (row block, chunk) pairs
 
     const int nsub_max = p.cpc * kChunkSubs < p.S_row ? p.cpc * kChunkSubs : p.S_row;
-    const SmemLayout L = smem_layout(BITS, V, nthreads >> 5, nsub_max, p.max_rb, p.cpc);
+    const SmemLayout L = smem_layout(BITS, V, nthreads >> 5, nsub_max, p.max_rb, p.cpc, XF32);
     const uint32_t xs = smem_u32(smem + L.xs);
     float *cvs = reinterpret_cast<float *>(smem + L.cv);
     unsigned *s_next = reinterpret_cast<unsigned *>(smem + L.misc);
@@ -1105,10 +1163,10 @@ __device__ __forceinline__ void qmv_direct_body(const Params &p)
     if (u0 < nunits) load_unit(u0, w_cur, s_cur, b_cur);
     grid_launch_dependents();
     grid_dependency_wait();  // x may be written by the preceding grid
-    stage_x<BITS, V>(smem, L.xs, p.x, p.K, sub_lo, nsub, nsub_max, tid, nthreads);
+    stage_x<BITS, V, XF32>(smem, L.xs, p.x, p.K, sub_lo, nsub, nsub_max, tid, nthreads);
     __syncthreads();
 
-    const uint32_t xv_bytes = uint32_t(nsub_max) * kXsB16;
+    const uint32_t xv_bytes = uint32_t(nsub_max) * xs_cell(XF32);
     const uint32_t wcell = smem_u32(smem + L.wbuf) + uint32_t(warp) * kRows * T::NP * 512u + uint32_t(lane) * 16u;
     while (u0 < nunits) {
         const Unit g = unit_geo(u0);
@@ -1131,19 +1189,19 @@ __device__ __forceinline__ void qmv_direct_body(const Params &p)
 #pragma unroll
         for (int ps = 0; ps < T::PASSES; ++ps) {
             const int v0 = ps * T::VP;
-            const uint32_t xsub = xs + (uint32_t(v0) * nsub_max + sl) * kXsB16;
+            const uint32_t xsub = xs + (uint32_t(v0) * nsub_max + sl) * xs_cell(XF32);
             uint64_t acc[kRows][T::VP];
             if constexpr (T::PASSES > 1)
-                subgroup_dot_vp_smem<BITS, T::VP>(wcell, xsub, xv_bytes, acc);
+                subgroup_dot_vp_smem<BITS, T::VP, XF32>(wcell, xsub, xv_bytes, acc);
             else
-                subgroup_dot_vp<BITS, T::VP>(w_cur, xsub, xv_bytes, acc);
+                subgroup_dot_vp<BITS, T::VP, XF32>(w_cur, xsub, xv_bytes, acc);
             float val[T::NRED];
 #pragma unroll
             for (int i = 0; i < T::NRED; ++i) val[i] = 0.0f;
 #pragma unroll
             for (int v = 0; v < T::VP; ++v) {
                 if (v0 + v >= V) break;
-                const float4 meta = lds_f4(xsub + v * xv_bytes + 128);
+                const float4 meta = lds_f4(xsub + v * xv_bytes + (XF32 ? 256 : 128));
 #pragma unroll
                 for (int r = 0; r < kRows; ++r) {
                     const float term = subgroup_term<true>(pair_lo(acc[r][v]), pair_hi(acc[r][v]), fs[r], fb[r], meta.x, meta.y, meta.z);
@@ -1185,10 +1243,11 @@ __global__ void __launch_bounds__(kThreadsV1, 1)
     qmv_ring_body<BITS, GS, SBP>(&map_w, &map_s, &map_b, p);
 }
 
-template <int BITS, int GS, int V, bool SBP>
+// XF32: x' staged as fp32 (else bf16).
+template <int BITS, int GS, int V, bool SBP, bool XF32>
 __global__ void __launch_bounds__(kThreadsVN, 1) qmv_streamed(const Params p)
 {
-    qmv_direct_body<BITS, GS, V, SBP>(p);
+    qmv_direct_body<BITS, GS, V, SBP, XF32>(p);
 }
 
 }  // namespace qmv

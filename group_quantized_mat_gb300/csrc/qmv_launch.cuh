@@ -51,9 +51,13 @@ cudaError_t launch_m1(const RingMaps &maps, const RingParams &p, const Launch &l
 template <int BITS, int GS, int V>
 cudaError_t launch_v(const Params &p, const Launch &l, cudaStream_t stream)
 {
-    static int configured[2][64] = {};
-    if (p.sb_packed) return launch_one(qmv_streamed<BITS, GS, V, true>, configured[1], l, stream, p);
-    return launch_one(qmv_streamed<BITS, GS, V, false>, configured[0], l, stream, p);
+    static int configured[4][64] = {};
+    if (p.sb_packed) {
+        if (p.xf32) return launch_one(qmv_streamed<BITS, GS, V, true, true>, configured[3], l, stream, p);
+        return launch_one(qmv_streamed<BITS, GS, V, true, false>, configured[2], l, stream, p);
+    }
+    if (p.xf32) return launch_one(qmv_streamed<BITS, GS, V, false, true>, configured[1], l, stream, p);
+    return launch_one(qmv_streamed<BITS, GS, V, false, false>, configured[0], l, stream, p);
 }
 
 template <int BITS, int GS>

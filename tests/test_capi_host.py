@@ -101,6 +101,7 @@ def test_split_plan(lib):
     assert g.qmv_workspace_size(1, 256, 1024, 4, 64) == 0
     # one CTA covers all chunks of its rows (no workspace) while the staged x
     # of all of K fits: M = 1 on both projections, M up to 16 on K = 3840
+    # (x' staged as bf16 there when fp32 would not fit all of K)
     assert g.qmv_workspace_size(1, 15360, 3840, 4, 64) == 0
     assert g.qmv_workspace_size(1, 3840, 15360, 4, 64) == 0
     assert g.qmv_workspace_size(13, 15360, 3840, 4, 64) == 0
