@@ -185,7 +185,7 @@ def qmv_run_ex(w_q, scales, biases, x, y, M: int, N: int, K: int, bits: int, gro
     _check(code, "qmv_run_ex")
 
 
-NOALLOC_SCRATCH_BYTES = 4 << 20
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 def qmv_run_noalloc(w_q, scales, biases, x, y, M: int, N: int, K: int, bits: int, group_size: int,

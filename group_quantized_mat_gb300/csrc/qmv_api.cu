@@ -236,10 +236,20 @@ Problem plan(int V, int N, int K, int bits, int gs, int sms, bool sb_packed = fa
 
 size_t counter_bytes(int NB) { return (size_t(NB) * sizeof(unsigned) + 255) & ~size_t(255); }
 
-size_t workspace_bytes_for(const Problem &pr)
+// Workspace of a launch: [counters][partials] when CTAs split K, then for the
+// streamed kernel the call's staged x cells [V][S_row]. Nothing in it carries
+// over between calls: each launch clears its tickets first.
+size_t split_bytes(const Problem &pr)
 {
     if (pr.cpc >= pr.ks) return 0;
     return counter_bytes(pr.NB) + size_t(pr.ks) * size_t(pr.V) * size_t(pr.N) * sizeof(float);
+}
+size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+size_t staged_offset(const Problem &pr) { return align256(split_bytes(pr)); }
+size_t workspace_bytes_for(const Problem &pr)
+{
+    if (pr.V < 2) return split_bytes(pr);
+    return staged_offset(pr) + align256(size_t(pr.V) * size_t(pr.S_row) * size_t(qmv::xs_cell(pr.xf32)));
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
@@ -364,6 +374,31 @@ cudaError_t dispatch(const Problem &pr, const qmv::RingMaps &maps, const qmv::Pa
     l.threads = pr.threads;
     l.smem = size_t(pr.smem);
     l.pdl = pdl;
+    if (pr.V >= 2) {
+        // the call's x staging first; the streamed kernel follows it with a
+        // programmatic dependency, so its weight loads overlap the staging
+        // (everything it writes, and the staged cells it reads, come after
+        // its wait for the staging grid, itself ordered after the stream's
+        // earlier work)
+        // (it also clears the K-split tickets)
+        uint8_t *cells = const_cast<uint8_t *>(p.xs_staged);
+        const int nc = p.counters ? pr.NB : 0;
+        cudaError_t e;
+        if (pr.bits == 4 && pr.gs == 64)
+            e = qmv::launch_b4g64_stage(pr.xf32, p.x, pr.K, pr.S_row, pr.V, cells, p.counters, nc, pdl, stream);
+        else if (pr.bits == 4)
+            e = qmv::launch_b4g128_stage(pr.xf32, p.x, pr.K, pr.S_row, pr.V, cells, p.counters, nc, pdl, stream);
+        else if (pr.gs == 64)
+            e = qmv::launch_b2g64_stage(pr.xf32, p.x, pr.K, pr.S_row, pr.V, cells, p.counters, nc, pdl, stream);
+        else
+            e = qmv::launch_b2g128_stage(pr.xf32, p.x, pr.K, pr.S_row, pr.V, cells, p.counters, nc, pdl, stream);
+        if (e != cudaSuccess) return e;
+        l.pdl = true;
+    } else if (p.counters) {
+        // a K-split one-vector launch: its tickets start at zero
+        cudaError_t e = cudaMemsetAsync(p.counters, 0, counter_bytes(pr.NB), stream);
+        if (e != cudaSuccess) return e;
+    }
     if (pr.V == 1) {
         qmv::RingParams rp;
         static_cast<qmv::Params &>(rp) = p;
@@ -463,9 +498,10 @@ qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t 
         p.f32_out = f32_out ? 1 : 0;
         p.sb_packed = sb_packed ? 1 : 0;
         p.xf32 = pr.xf32;
-        const bool split = workspace_bytes_for(pr) > 0;
+        const bool split = split_bytes(pr) > 0;
         p.counters = split ? static_cast<unsigned *>(workspace) : nullptr;
         p.partials = split ? reinterpret_cast<float *>(static_cast<char *>(workspace) + counter_bytes(pr.NB)) : nullptr;
+        p.xs_staged = V >= 2 ? static_cast<const uint8_t *>(workspace) + staged_offset(pr) : nullptr;
         for (int m = m_lo; m < m_hi; m += V) {
             p.x = x + size_t(m) * K;
             p.y = static_cast<char *>(y) + size_t(m) * N * ysize;

@@ -625,49 +625,49 @@ __device__ __forceinline__ int octet_position(int t, int e8)
     return BITS == 4 ? (e8 ^ (((t >> 2) & 1) * 4)) : e8;
 }
 
-// Stages x of subgroups [sub_lo, sub_lo + nsub) of every vector at smem + xs_off,
-// loading it from global memory (the streamed kernel): eight threads per
-// subgroup, eight elements each; threads [0, nthreads) of the CTA take part.
-// Each subgroup is xs_cell(XF32) bytes: its 64 x' (octets in processing
-// order) as fp32 (the values are exactly the bf16 x') or as bf16, then
-// (sx, f1, f2, 0). fp32 spares the datapath the unpacking of bf16 pairs, once
-// per vector and octet; bf16 takes half the shared memory.
-template <int BITS, int V, bool XF32>
-__device__ __forceinline__ void stage_x(uint8_t *smem, int xs_off, const uint16_t *x, int K, int sub_lo, int nsub,
-                                        int nsub_max, int tid, int nthreads)
+// Writes eighth e8 of subgroup t (its staged x' and, from e8 = 0, the
+// subgroup's (sx, f1, f2, 0)) into the streamed kernel's cell: xs_cell(XF32)
+// bytes, its 64 x' (octets in processing order) as fp32 -- exactly the bf16
+// values, so the datapath unpacks nothing -- or as bf16 (half the space),
+// then the meta.
+template <int BITS, bool XF32>
+__device__ __forceinline__ void write_cell(uint8_t *cell, int t, int e8, const uint4 &packed, const float4 &meta)
 {
-    const int per_vec = nsub * 8, all = V * per_vec;
-    const int all_pad = (all + nthreads - 1) / nthreads * nthreads;
-    // kB tasks of a thread at a time: their dependent chains (the exponent
-    // maximum, the scaling, the eight-lane sum) overlap
-    constexpr int kB = 4;
-    for (int u0 = tid; u0 < all_pad; u0 += kB * nthreads) {
-#pragma unroll
-        for (int b = 0; b < kB; ++b) {
-            const int u = u0 + b * nthreads;
-            const bool live = u < all;  // uniform over each eight-lane group; dead tasks only shuffle
-            const int v = live ? u / per_vec : 0;
-            const int rem = live ? u - v * per_vec : 0;
-            const int sl = rem >> 3, e8 = rem & 7;  // subgroup (CTA-local), eighth
-            uint4 raw = make_uint4(0, 0, 0, 0);
-            if (live)
-                raw = __ldg(reinterpret_cast<const uint4 *>(x + size_t(v) * K + size_t(sub_lo + sl) * kSub) + e8);
-            uint4 packed;
-            float4 meta;
-            stage_eight<BITS, false>(raw, packed, meta);
-            if (live) {
-                uint8_t *cell = smem + xs_off + (size_t(v) * nsub_max + sl) * xs_cell(XF32);
-                if constexpr (XF32) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(cell + octet_position<BITS>(sub_lo + sl, e8) * 32);
-                    dst[0] = make_uint4(packed.x << 16, packed.x & 0xFFFF0000u, packed.y << 16, packed.y & 0xFFFF0000u);
-                    dst[1] = make_uint4(packed.z << 16, packed.z & 0xFFFF0000u, packed.w << 16, packed.w & 0xFFFF0000u);
-                } else {
-                    *reinterpret_cast<uint4 *>(cell + octet_position<BITS>(sub_lo + sl, e8) * 16) = packed;
-                }
-                if (e8 == 0) *reinterpret_cast<float4 *>(cell + (XF32 ? 256 : 128)) = meta;
-            }
-        }
+    if constexpr (XF32) {
+        uint4 *dst = reinterpret_cast<uint4 *>(cell + octet_position<BITS>(t, e8) * 32);
+        dst[0] = make_uint4(packed.x << 16, packed.x & 0xFFFF0000u, packed.y << 16, packed.y & 0xFFFF0000u);
+        dst[1] = make_uint4(packed.z << 16, packed.z & 0xFFFF0000u, packed.w << 16, packed.w & 0xFFFF0000u);
+    } else {
+        *reinterpret_cast<uint4 *>(cell + octet_position<BITS>(t, e8) * 16) = packed;
     }
+    if (e8 == 0) *reinterpret_cast<float4 *>(cell + (XF32 ? 256 : 128)) = meta;
+}
+
+// Steps 1 and 2 for every vector, once per call, for the streamed kernel:
+// cell (v, t) of vector v and subgroup t at out + (v * S_row + t) * cell
+// bytes. Eight threads per subgroup (the grid is a whole number of warps;
+// threads past the end only take part in the shuffles).
+template <int BITS, bool XF32>
+__device__ __forceinline__ void stage_all_body(const uint16_t *x, int K, int S_row, int V, uint8_t *out,
+                                               unsigned *counters, int ncounters)
+{
+    grid_launch_dependents();  // the streamed kernel may start loading weights
+    grid_dependency_wait();    // x may be written by the preceding grid
+    // the K-split tickets of the streamed kernel start at zero
+    for (int i = int(blockIdx.x) * int(blockDim.x) + int(threadIdx.x); i < ncounters; i += int(gridDim.x * blockDim.x))
+        counters[i] = 0u;
+    const int per_vec = S_row * 8, all = V * per_vec;
+    const int u = int(blockIdx.x) * int(blockDim.x) + int(threadIdx.x);
+    const bool live = u < all;  // uniform over each eight-lane group
+    const int v = live ? u / per_vec : 0;
+    const int rem = live ? u - v * per_vec : 0;
+    const int t = rem >> 3, e8 = rem & 7;
+    uint4 raw = make_uint4(0, 0, 0, 0);
+    if (live) raw = __ldg(reinterpret_cast<const uint4 *>(x + size_t(v) * K + size_t(t) * kSub) + e8);
+    uint4 packed;
+    float4 meta;
+    stage_eight<BITS, false>(raw, packed, meta);
+    if (live) write_cell<BITS, XF32>(out + (size_t(v) * S_row + t) * xs_cell(XF32), t, e8, packed, meta);
 }
 
 // Stages x (one vector) for the one-vector kernel in place: the raw bf16 x of
@@ -724,8 +724,9 @@ __device__ __forceinline__ float chunk_v1(const uint4 (&quads)[kRows][BITS == 4 
 // Step 4 and the output: fold the chunk values of the CTA's rows (cvs, laid
 // out [row][chunk][vector]) left to right into y -- directly when the CTA
 // covers all chunks, else through the workspace, the CTA that completes a row
-// range last folding all chunks (and zeroing what it read, so the workspace
-// is zero again).
+// range last folding all chunks. Every partial it reads was written by this
+// call; the range's ticket counter starts at zero (the launch clears it) and
+// returns to zero.
 template <int V>
 __device__ __forceinline__ void fold_chunks(const float *cvs, int nrows, int row_t0, int c_lo, int cpc_here, int rb_lo,
                                             int tid, int nthreads, int N, int ks, int cpc, float *partials,
@@ -798,7 +799,6 @@ __device__ __forceinline__ void fold_chunks(const float *cvs, int nrows, int row
             const int idx = base + u * nthreads;
             const int v = idx / nrows;
             store_y(v, int(off[u] - size_t(v) * N), acc[u]);
-            for (int c = 0; c < ks; ++c) __stcg(partials + size_t(c) * plane + off[u], 0.0f);  // zero again
         }
     }
 }
@@ -1105,7 +1105,12 @@ __device__ __forceinline__ void qmv_direct_body(const Params &p)
     const uint32_t xs = smem_u32(smem + L.xs);
     float *cvs = reinterpret_cast<float *>(smem + L.cv);
     unsigned *s_next = reinterpret_cast<unsigned *>(smem + L.misc);
-    if (tid == 0) *s_next = 0;
+    const uint32_t xbar = smem_u32(smem + L.misc + 8);
+    if (tid == 0) {
+        *s_next = 0;
+        mbar_init(xbar, 1);
+        fence_mbar_init();
+    }
     __syncthreads();
 
     uint32_t poff[T::NP];
@@ -1155,16 +1160,30 @@ __device__ __forceinline__ void qmv_direct_body(const Params &p)
         }
     };
 
-    // The first unit's loads first: they do not depend on the preceding grid,
-    // so their latency overlaps its tail and the staging of x below.
+    // The first unit's loads first: they do not depend on the preceding grid
+    // (the call's staging kernel), so their latency overlaps it.
     int u0 = grab();
     uint4 w_cur[kRows][T::NP];
     uint32_t s_cur[kRows] = {0, 0, 0, 0}, b_cur[kRows] = {0, 0, 0, 0};
     if (u0 < nunits) load_unit(u0, w_cur, s_cur, b_cur);
     grid_launch_dependents();
-    grid_dependency_wait();  // x may be written by the preceding grid
-    stage_x<BITS, V, XF32>(smem, L.xs, p.x, p.K, sub_lo, nsub, nsub_max, tid, nthreads);
-    __syncthreads();
+    grid_dependency_wait();  // the staged cells are written by the preceding grid
+    constexpr uint32_t kCell = xs_cell(XF32);
+    if (tid == 0) {
+        // this CTA's subgroups of every vector: one bulk copy per vector
+        mbar_arrive_expect_tx(xbar, uint32_t(V * nsub) * kCell);
+        for (int v = 0; v < V; ++v)
+            bulk_load_plain(xs + uint32_t(v * nsub_max) * kCell, p.xs_staged + (size_t(v) * p.S_row + sub_lo) * kCell,
+                            uint32_t(nsub) * kCell, xbar);
+    }
+    if (__syncthreads_or(!mbar_wait_bounded(xbar, 0))) {
+        if (tid == 0) {
+            atomicOr(p.err, 1u);
+            (void)mbar_wait_bounded(xbar, 0);  // the copies may still be landing
+        }
+        __syncthreads();
+        return;
+    }
 
     const uint32_t xv_bytes = uint32_t(nsub_max) * xs_cell(XF32);
     const uint32_t wcell = smem_u32(smem + L.wbuf) + uint32_t(warp) * kRows * T::NP * 512u + uint32_t(lane) * 16u;
@@ -1248,6 +1267,15 @@ template <int BITS, int GS, int V, bool SBP, bool XF32>
 __global__ void __launch_bounds__(kThreadsVN, 1) qmv_streamed(const Params p)
 {
     qmv_direct_body<BITS, GS, V, SBP, XF32>(p);
+}
+
+// The streamed kernel's x staging, once per call (kStageThreads a block).
+constexpr int kStageThreads = 128;
+template <int BITS, bool XF32>
+__global__ void __launch_bounds__(kStageThreads)
+    qmv_stage_x(const uint16_t *x, int K, int S_row, int V, uint8_t *out, unsigned *counters, int ncounters)
+{
+    stage_all_body<BITS, XF32>(x, K, S_row, V, out, counters, ncounters);
 }
 
 }  // namespace qmv

@@ -60,6 +60,23 @@ cudaError_t launch_v(const Params &p, const Launch &l, cudaStream_t stream)
     return launch_one(qmv_streamed<BITS, GS, V, false, false>, configured[0], l, stream, p);
 }
 
+// The call's x staging for the streamed kernel (one thread per eight
+// elements of a vector).
+template <int BITS>
+cudaError_t launch_stage(bool xf32, const uint16_t *x, int K, int S_row, int V, uint8_t *out, unsigned *counters,
+                         int ncounters, bool pdl, cudaStream_t stream)
+{
+    static int configured[2][64] = {};
+    const long long threads = (long long)V * S_row * 8;
+    Launch l;
+    l.grid = dim3(unsigned((threads + kStageThreads - 1) / kStageThreads));
+    l.threads = kStageThreads;
+    l.smem = 0;
+    l.pdl = pdl;
+    if (xf32) return launch_one(qmv_stage_x<BITS, true>, configured[1], l, stream, x, K, S_row, V, out, counters, ncounters);
+    return launch_one(qmv_stage_x<BITS, false>, configured[0], l, stream, x, K, S_row, V, out, counters, ncounters);
+}
+
 template <int BITS, int GS>
 cudaError_t launch_streamed(int V, const Params &p, const Launch &l, cudaStream_t stream)
 {

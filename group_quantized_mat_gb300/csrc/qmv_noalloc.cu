@@ -19,7 +19,7 @@ namespace {
 
 // Scratch shared by every qmv_run_noalloc call on a device. Each GPU that
 // loads this library holds QMV_NOALLOC_SCRATCH_BYTES of it until the process
-// exits. It keeps whatever the last call left in it.
+// exits. It keeps whatever the last call left in it, which no call reads.
 __device__ __align__(256) unsigned char g_noalloc_scratch[QMV_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
@@ -57,10 +57,8 @@ extern "C" qmv_status qmv_run_noalloc(const uint32_t *w_q, const uint16_t *scale
     void *scratch = nullptr;
     qmv_status st = scratch_address(dev, &scratch);
     if (st != QMV_OK) return st;
-    // The K-split counters and partial sums must start at zero; the array keeps
-    // the previous call's contents, so clear the part this call uses.
-    if (cudaMemsetAsync(scratch, 0, need, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return QMV_ERR_CUDA;
+    // The array keeps whatever the previous call left; a call needs nothing
+    // of it (each launch clears its own K-split tickets).
     return qmv_run_ex(w_q, scales, biases, x, y, M, N, K, bits, group_size, scratch, QMV_NOALLOC_SCRATCH_BYTES, 0u,
                       stream);
 }

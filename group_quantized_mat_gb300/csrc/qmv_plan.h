@@ -54,6 +54,7 @@ struct Params {
     int max_rb;               // row blocks of the largest CTA share
     int f32_out;
     int xf32;                 // streamed kernel: x' staged as fp32 (else bf16)
+    const uint8_t *xs_staged; // streamed kernel: the call's staged cells [V][S_row] (qmv_stage_x)
     int sb_packed;            // 1: scales is the interleaved uint32 array (scale low, bias high), biases unused
 };
 
@@ -94,7 +95,7 @@ __host__ __device__ inline SmemLayout smem_layout(int bits, int V, int warps, in
     L.cv = align_up(V * nsub * xs_cell(xf32), 16);
     L.wbuf = align_up(L.cv + max_rb * kRows * cpc * V * 4, 16);
     L.misc = L.wbuf + (vectors_per_pass(V) < V ? warps * kRows * 32 * sub_bytes(bits) : 0);
-    L.total = L.misc + 16 + 128;  // next-unit counter; slack for aligning the dynamic base
+    L.total = L.misc + 16 + 128;  // next-unit counter and the x barrier; slack for aligning the dynamic base
     return L;
 }
 

@@ -112,8 +112,11 @@ QMV_API qmv_status qmv_pack_sb(const uint16_t *scales, const uint16_t *biases, u
  * guarantee below). */
 QMV_API int qmv_split_count(int N, int K, int bits, int group_size);
 
-/* Bytes of device workspace a call with these arguments needs (0 when one CTA
- * covers all K-chunks of its rows). Returns 0 for invalid arguments too. */
+/* Bytes of device workspace a call with these arguments needs: for M >= 2 the
+ * call's staged activations (M x K/64 cells of 144 or 272 bytes), plus, when
+ * CTAs split K, one counter per 4-row block and the per-chunk partial sums
+ * (0 for M = 1 when one CTA covers all K-chunks of its rows). Returns 0 for
+ * invalid arguments too. */
 QMV_API size_t qmv_workspace_size(int M, int N, int K, int bits, int group_size);
 
 /* ------------------------------------------------------------------- run */
@@ -168,11 +171,11 @@ QMV_API qmv_status qmv_run(const uint32_t *w_q, const uint16_t *scales, const ui
  *
  *  workspace        device, 16-byte aligned, at least qmv_workspace_size(M, N, K,
  *                   bits, group_size) bytes, or NULL to use the library workspace.
- *                   It must be all zero before its first use (qmv_workspace_init
- *                   or cudaMemset); every completed call leaves it all zero again,
- *                   so one workspace serves any sequence of problem shapes. Calls
- *                   sharing one workspace must not overlap on the GPU. After a
- *                   device error (qmv_device_error) zero it again.
+ *                   Scratch only: a call needs no particular contents (it clears
+ *                   what must start at zero on `stream` itself) and leaves
+ *                   unspecified ones, so one workspace serves any sequence of
+ *                   problem shapes. Calls sharing one workspace must not overlap
+ *                   on the GPU.
  *  workspace_bytes  its size in bytes (ignored when workspace is NULL).
  *  flags            bitwise OR of QMV_* flags above.
  * Additional errors: QMV_ERR_WORKSPACE, QMV_ERR_FLAGS. */
@@ -181,8 +184,8 @@ QMV_API qmv_status qmv_run_ex(const uint32_t *w_q, const uint16_t *scales, const
                       int group_size, void *workspace, size_t workspace_bytes,
                       unsigned flags, qmv_stream_t stream);
 
-/* Size of the fixed scratch array behind qmv_run_noalloc (4 MiB per device). */
-#define QMV_NOALLOC_SCRATCH_BYTES (4u << 20)
+/* Size of the fixed scratch array behind qmv_run_noalloc (8 MiB per device). */
+#define QMV_NOALLOC_SCRATCH_BYTES (8u << 20)
 
 /* qmv_run without any device allocation. The paper has no counterpart: this
  * entry point exists for callers that cannot call cudaMalloc -- code running
@@ -197,8 +200,7 @@ QMV_API qmv_status qmv_run_ex(const uint32_t *w_q, const uint16_t *scales, const
  * of qmv_run. The scratch that K-split problems need comes from one static
  * device array of QMV_NOALLOC_SCRATCH_BYTES that every GPU loading the library
  * holds until exit; no cudaMalloc, cudaFree or allocating library routine is
- * called. Each call clears the part of it that must start at zero
- * (cudaMemsetAsync on `stream`). All calls on a device share the array, so
+ * called. All calls on a device share the array, so
  * calls that overlap on the GPU (other streams, or concurrent host threads)
  * race and give undefined results.
  *
@@ -212,7 +214,9 @@ QMV_API qmv_status qmv_run_noalloc(const uint32_t *w_q, const uint16_t *scales, 
                                    const uint16_t *x, uint16_t *y, int M, int N, int K, int bits,
                                    int group_size, qmv_stream_t stream);
 
-/* Zero-fills `bytes` of a caller workspace on `stream` (cudaMemsetAsync). */
+/* Zero-fills `bytes` of a caller workspace on `stream` (cudaMemsetAsync). Calls
+ * do not need it (a workspace holds no state between calls); kept as a
+ * convenience. */
 QMV_API qmv_status qmv_workspace_init(void *workspace, size_t bytes, qmv_stream_t stream);
 
 /* ------------------------------------------------------------ diagnostics */

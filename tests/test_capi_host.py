@@ -98,23 +98,28 @@ def test_split_plan(lib):
     assert g.qmv_split_count(3840, 15360, 4, 64) == 8
     assert g.qmv_split_count(5120, 17408, 4, 64) == 9
     assert g.qmv_split_count(1, 1000, 4, 64) == 0
+    a256 = lambda b: (b + 255) // 256 * 256
+    # M = 1: no workspace while one CTA covers all chunks of its rows
     assert g.qmv_workspace_size(1, 256, 1024, 4, 64) == 0
-    # one CTA covers all chunks of its rows (no workspace) while the staged x
-    # of all of K fits: M = 1 on both projections, M up to 16 on K = 3840
-    # (x' staged as bf16 there when fp32 would not fit all of K)
     assert g.qmv_workspace_size(1, 15360, 3840, 4, 64) == 0
     assert g.qmv_workspace_size(1, 3840, 15360, 4, 64) == 0
-    assert g.qmv_workspace_size(13, 15360, 3840, 4, 64) == 0
-    assert g.qmv_workspace_size(16, 15360, 3840, 4, 64) == 0
-    # otherwise a range of chunks per CTA; chunk values meet in the workspace
-    # after a 256-byte-aligned block of one counter per 4-row block
+    # M >= 2: the call's staged x cells [M][K/64] (144 bytes with bf16 x',
+    # 272 with fp32 x'). On K = 3840 bf16 cells let a CTA take all of K, so
+    # there is no K split; fp32 cells would have forced one.
+    assert g.qmv_workspace_size(13, 15360, 3840, 4, 64) == a256(13 * 60 * 144)
+    assert g.qmv_workspace_size(16, 15360, 3840, 4, 64) == a256(16 * 60 * 144)
+    assert g.qmv_workspace_size(2, 15360, 3840, 4, 64) == a256(2 * 60 * 272)
+    # K = 15360 splits either way, so fp32 cells; chunk values meet in the
+    # workspace first: a 256-byte-aligned block of one counter per 4-row
+    # block, then ks x M x N fp32 partials, then the cells
+    split13 = (960 * 4 + 255) // 256 * 256 + 8 * 13 * 3840 * 4
     w13 = g.qmv_workspace_size(13, 3840, 15360, 4, 64)
-    assert w13 == (960 * 4 + 255) // 256 * 256 + 8 * 13 * 3840 * 4
+    assert w13 == a256(split13) + a256(13 * 240 * 272)
     w16 = g.qmv_workspace_size(16, 3840, 15360, 4, 64)
-    assert w16 - w13 == 8 * 3 * 3840 * 4
+    assert w16 == a256(split13 + 8 * 3 * 3840 * 4) + a256(16 * 240 * 272)
     # M above 16 runs as launches of 16 vectors and one of the remainder: the
     # widest of those decides
-    assert g.qmv_workspace_size(17, 15360, 3840, 4, 64) == 0
+    assert g.qmv_workspace_size(17, 15360, 3840, 4, 64) == a256(16 * 60 * 144)
     assert g.qmv_workspace_size(20, 3840, 15360, 4, 64) == w16
     assert g.qmv_workspace_size(33, 3840, 15360, 4, 64) == w16
     assert g.qmv_workspace_size(256, 3840, 15360, 4, 64) == w16

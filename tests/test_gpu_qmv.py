@@ -253,7 +253,7 @@ def test_cuda_graph_capture_replays_identically():
 
 def test_workspace_serves_any_shape_sequence():
     """One workspace, problems of different N / K / M in turn: every call must
-    match a fresh-workspace result, and the workspace must be zero afterwards."""
+    match a fresh-workspace result whatever the workspace held before."""
     probs = [DeviceProblem(synth.make_inputs(3840, 15360, 16, 4, 64, seed=21)),
              DeviceProblem(synth.make_inputs(5120, 5120, 13, 4, 64, seed=22)),
              DeviceProblem(synth.make_inputs(1000, 3840, 3, 2, 128, seed=23))]
@@ -263,10 +263,11 @@ def test_workspace_serves_any_shape_sequence():
         nb = g.qmv_workspace_size(p.M, p.N, p.K, p.bits, p.gs)
         fresh = torch.zeros(nb // 4 + 4, dtype=torch.int32, device="cuda")
         refs.append(p.run(flags=g.F32_OUT, workspace=fresh, workspace_bytes=nb))
-    ws = torch.zeros(need // 4 + 4, dtype=torch.int32, device="cuda")
+    # the workspace is scratch: garbage left in it (here, random words) must
+    # not change any result
+    ws = torch.randint(-2**31, 2**31 - 1, (need // 4 + 4,), dtype=torch.int32, device="cuda")
     for rnd in range(2):
         for p, ref in zip(probs, refs):
             y = p.run(flags=g.F32_OUT, workspace=ws, workspace_bytes=need)
             assert np.array_equal(y.view(np.uint32), ref.view(np.uint32)), f"round {rnd} N={p.N}"
-    torch.cuda.synchronize()
-    assert int(torch.count_nonzero(ws)) == 0
+        ws.random_(-2**31, 2**31 - 1)
