@@ -69,7 +69,6 @@ struct Problem {
     // one-vector ring
     int uc, unit_mode, pitch, sb_mode_unit, sbox, slots, consumers;
     int sb_packed;
-    int xf32;       // streamed kernel: fp32 staging of x'
 };
 
 // Largest dynamic shared memory a CTA may use (static shared memory and
@@ -84,7 +83,7 @@ constexpr int kMaxSlots = 24;
 
 #if defined(QMV_TUNING)
 // Tuning builds only: fixed launch shapes for sweeps (0 = automatic).
-struct TuneOverride { int slots = 0, uc = 0, consumers = 0, grid_rows = 0, cpc = 0, xf32 = -1; };
+struct TuneOverride { int slots = 0, uc = 0, consumers = 0, grid_rows = 0, cpc = 0; };
 TuneOverride g_tune;
 #endif
 
@@ -117,12 +116,10 @@ void grid_shape(Problem &pr, int sms, int V, int cv_bytes)
     pr.max_rb = (pr.NB + gr - 1) / gr;
 }
 
-// Streamed kernel (V >= 2): all of K per CTA (no workspace) when the staged
-// x fits, else the widest chunk range that fits (one chunk always does). x' is
-// staged as fp32 unless that needs a narrower range than bf16 would while
-// bf16 covers all of K (the split then costs more than the unpacking saves).
-// Whether a workspace is needed never depends on `sms` (the fit is checked
-// against the chunk-value cap), so qmv_workspace_size needs no GPU.
+// Streamed kernel (V >= 2): all of K per CTA (no K split) when the x cells
+// of all of K fit, else the widest chunk range that fits (one chunk always
+// does). Whether the K split happens never depends on `sms` (the fit is
+// checked against the chunk-value cap), so qmv_workspace_size needs no GPU.
 Problem plan_direct(int V, int N, int K, int bits, int gs, int sms)
 {
     Problem pr{};
@@ -130,26 +127,17 @@ Problem plan_direct(int V, int N, int K, int bits, int gs, int sms)
     const int warps = qmv::kStreamedWarps;
     const int wbuf = qmv::vectors_per_pass(V) < V ? warps * qmv::kRows * 32 * qmv::sub_bytes(bits) : 0;
     auto nsub_of = [&](int cpc) { return cpc * qmv::kChunkSubs < pr.S_row ? cpc * qmv::kChunkSubs : pr.S_row; };
-    auto xs_bytes = [&](int cpc, bool xf32) { return qmv::align_up(V * nsub_of(cpc) * qmv::xs_cell(xf32), 16); };
-    auto widest = [&](bool xf32) {
-        int cpc = pr.ks;
-        while (cpc > 1 && xs_bytes(cpc, xf32) + kCvBudget + wbuf + 16 + 128 > kSmemBudget) --cpc;
-        return cpc;
-    };
-    const int cpc32 = widest(true), cpc16 = widest(false);
-    pr.xf32 = (cpc32 == pr.ks || cpc16 < pr.ks) ? 1 : 0;
-#if defined(QMV_TUNING)
-    if (g_tune.xf32 >= 0) pr.xf32 = g_tune.xf32;
-#endif
-    pr.cpc = pr.xf32 ? cpc32 : cpc16;
+    auto xs_bytes = [&](int cpc) { return qmv::align_up(V * nsub_of(cpc) * qmv::kXsF32, 16); };
+    pr.cpc = pr.ks;
+    while (pr.cpc > 1 && xs_bytes(pr.cpc) + kCvBudget + wbuf + 16 + 128 > kSmemBudget) --pr.cpc;
 #if defined(QMV_TUNING)
     if (g_tune.cpc > 0 && g_tune.cpc <= pr.ks) pr.cpc = g_tune.cpc;
 #endif
     pr.threads = 32 * warps;
-    // chunk values may use whatever shared memory the staged x and the
-    // weight buffer leave (at least kCvBudget, by the fit above)
-    grid_shape(pr, sms, V, kSmemBudget - (xs_bytes(pr.cpc, pr.xf32) + wbuf + 16 + 128 + 16));
-    pr.smem = qmv::smem_layout(bits, V, warps, nsub_of(pr.cpc), pr.max_rb, pr.cpc, pr.xf32).total;
+    // chunk values may use whatever shared memory the x cells and the weight
+    // buffer leave (at least kCvBudget, by the fit above)
+    grid_shape(pr, sms, V, kSmemBudget - (xs_bytes(pr.cpc) + wbuf + 16 + 128 + 16));
+    pr.smem = qmv::smem_layout(bits, V, warps, nsub_of(pr.cpc), pr.max_rb, pr.cpc).total;
     return pr;
 }
 
@@ -249,7 +237,7 @@ size_t staged_offset(const Problem &pr) { return align256(split_bytes(pr)); }
 size_t workspace_bytes_for(const Problem &pr)
 {
     if (pr.V < 2) return split_bytes(pr);
-    return staged_offset(pr) + align256(size_t(pr.V) * size_t(pr.S_row) * size_t(qmv::xs_cell(pr.xf32)));
+    return staged_offset(pr) + align256(size_t(pr.V) * size_t(pr.S_row) * size_t(qmv::kXsF32));
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
@@ -385,13 +373,13 @@ cudaError_t dispatch(const Problem &pr, const qmv::RingMaps &maps, const qmv::Pa
         const int nc = p.counters ? pr.NB : 0;
         cudaError_t e;
         if (pr.bits == 4 && pr.gs == 64)
-            e = qmv::launch_b4g64_stage(pr.xf32, p.x, pr.K, pr.S_row, pr.V, cells, p.counters, nc, pdl, stream);
+            e = qmv::launch_b4g64_stage(p.x, pr.K, pr.S_row, pr.V, cells, p.counters, nc, pdl, stream);
         else if (pr.bits == 4)
-            e = qmv::launch_b4g128_stage(pr.xf32, p.x, pr.K, pr.S_row, pr.V, cells, p.counters, nc, pdl, stream);
+            e = qmv::launch_b4g128_stage(p.x, pr.K, pr.S_row, pr.V, cells, p.counters, nc, pdl, stream);
         else if (pr.gs == 64)
-            e = qmv::launch_b2g64_stage(pr.xf32, p.x, pr.K, pr.S_row, pr.V, cells, p.counters, nc, pdl, stream);
+            e = qmv::launch_b2g64_stage(p.x, pr.K, pr.S_row, pr.V, cells, p.counters, nc, pdl, stream);
         else
-            e = qmv::launch_b2g128_stage(pr.xf32, p.x, pr.K, pr.S_row, pr.V, cells, p.counters, nc, pdl, stream);
+            e = qmv::launch_b2g128_stage(p.x, pr.K, pr.S_row, pr.V, cells, p.counters, nc, pdl, stream);
         if (e != cudaSuccess) return e;
         l.pdl = true;
     } else if (p.counters) {
@@ -497,7 +485,6 @@ qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t 
         p.NB = pr.NB; p.grid_rows = pr.grid_rows; p.cpc = pr.cpc; p.max_rb = pr.max_rb;
         p.f32_out = f32_out ? 1 : 0;
         p.sb_packed = sb_packed ? 1 : 0;
-        p.xf32 = pr.xf32;
         const bool split = split_bytes(pr) > 0;
         p.counters = split ? static_cast<unsigned *>(workspace) : nullptr;
         p.partials = split ? reinterpret_cast<float *>(static_cast<char *>(workspace) + counter_bytes(pr.NB)) : nullptr;
@@ -530,7 +517,6 @@ extern "C" __attribute__((visibility("default"))) void qmv_tune_set(int slots, i
     g_tune.grid_rows = grid_rows;
     g_tune.cpc = cpc;
 }
-extern "C" __attribute__((visibility("default"))) void qmv_tune_xf32(int xf32) { g_tune.xf32 = xf32; }
 #endif
 
 extern "C" size_t qmv_workspace_size(int M, int N, int K, int bits, int group_size)

@@ -10,9 +10,9 @@ cudaError_t launch_b2g64_streamed(int V, const Params &p, const Launch &l, cudaS
 {
     return launch_streamed<2, 64>(V, p, l, stream);
 }
-cudaError_t launch_b2g64_stage(bool xf32, const uint16_t *x, int K, int S_row, int V, uint8_t *out,
-                             unsigned *counters, int ncounters, bool pdl, cudaStream_t stream)
+cudaError_t launch_b2g64_stage(const uint16_t *x, int K, int S_row, int V, uint8_t *out, unsigned *counters,
+                             int ncounters, bool pdl, cudaStream_t stream)
 {
-    return launch_stage<2>(xf32, x, K, S_row, V, out, counters, ncounters, pdl, stream);
+    return launch_stage<2>(x, K, S_row, V, out, counters, ncounters, pdl, stream);
 }
 }  // namespace qmv

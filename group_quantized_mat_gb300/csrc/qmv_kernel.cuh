@@ -437,9 +437,9 @@ __device__ __forceinline__ void subgroup_dot_v1(const uint4 (&quads)[kRows][BITS
 }
 
 // Step 1 for VP vectors: acc[r][v].
-//   xsub   shared address of vector 0's staged subgroup (octet o at 32 * o
-//          for fp32 x', 16 * o for bf16 x'); xv bytes between vectors.
-template <int BITS, int VP, bool XF32>
+//   xsub   shared address of vector 0's staged subgroup (fp32 x', octet o at
+//          32 * o); xv bytes between vectors.
+template <int BITS, int VP>
 __device__ __forceinline__ void subgroup_dot_vp(const uint4 (&quads)[kRows][BITS == 4 ? 2 : 1], uint32_t xsub,
                                                 uint32_t xv, uint64_t (&acc)[kRows][VP])
 {
@@ -455,16 +455,8 @@ __device__ __forceinline__ void subgroup_dot_vp(const uint4 (&quads)[kRows][BITS
 #pragma unroll
         for (int v = 0; v < VP; ++v) {
             uint64_t x01, x23, x45, x67;
-            if constexpr (XF32) {
-                lds_v2_u64(xsub + v * xv + o * 32, x01, x23);
-                lds_v2_u64(xsub + v * xv + o * 32 + 16, x45, x67);
-            } else {
-                const uint4 xb = lds_v4_u32(xsub + v * xv + o * 16);
-                x01 = pack2(xb.x << 16, xb.x & 0xFFFF0000u);
-                x23 = pack2(xb.y << 16, xb.y & 0xFFFF0000u);
-                x45 = pack2(xb.z << 16, xb.z & 0xFFFF0000u);
-                x67 = pack2(xb.w << 16, xb.w & 0xFFFF0000u);
-            }
+            lds_v2_u64(xsub + v * xv + o * 32, x01, x23);
+            lds_v2_u64(xsub + v * xv + o * 32 + 16, x45, x67);
 #pragma unroll
             for (int r = 0; r < kRows; ++r) {
                 acc[r][v] = ffma2(q[r][0], x01, acc[r][v]);
@@ -478,7 +470,7 @@ __device__ __forceinline__ void subgroup_dot_vp(const uint4 (&quads)[kRows][BITS
 
 // subgroup_dot_vp with the weight bytes re-read from shared memory (cell
 // (r, pc) of this lane at wcell + (r*NP + pc) * 512), for two-pass V.
-template <int BITS, int VP, bool XF32>
+template <int BITS, int VP>
 __device__ __forceinline__ void subgroup_dot_vp_smem(uint32_t wcell, uint32_t xsub, uint32_t xv,
                                                      uint64_t (&acc)[kRows][VP])
 {
@@ -488,7 +480,7 @@ __device__ __forceinline__ void subgroup_dot_vp_smem(uint32_t wcell, uint32_t xs
     for (int r = 0; r < kRows; ++r)
 #pragma unroll
         for (int pc = 0; pc < NP; ++pc) quads[r][pc] = lds_v4_u32(wcell + uint32_t(r * NP + pc) * 512u);
-    subgroup_dot_vp<BITS, VP, XF32>(quads, xsub, xv, acc);
+    subgroup_dot_vp<BITS, VP>(quads, xsub, xv, acc);
 }
 
 // Step 2: the subgroup's term from its pair sums.
@@ -626,28 +618,23 @@ __device__ __forceinline__ int octet_position(int t, int e8)
 }
 
 // Writes eighth e8 of subgroup t (its staged x' and, from e8 = 0, the
-// subgroup's (sx, f1, f2, 0)) into the streamed kernel's cell: xs_cell(XF32)
-// bytes, its 64 x' (octets in processing order) as fp32 -- exactly the bf16
-// values, so the datapath unpacks nothing -- or as bf16 (half the space),
-// then the meta.
-template <int BITS, bool XF32>
+// subgroup's (sx, f1, f2, 0)) into the streamed kernel's kXsF32-byte cell:
+// its 64 x' (octets in processing order) as fp32 -- exactly the bf16 values,
+// so the datapath unpacks nothing -- then the meta.
+template <int BITS>
 __device__ __forceinline__ void write_cell(uint8_t *cell, int t, int e8, const uint4 &packed, const float4 &meta)
 {
-    if constexpr (XF32) {
-        uint4 *dst = reinterpret_cast<uint4 *>(cell + octet_position<BITS>(t, e8) * 32);
-        dst[0] = make_uint4(packed.x << 16, packed.x & 0xFFFF0000u, packed.y << 16, packed.y & 0xFFFF0000u);
-        dst[1] = make_uint4(packed.z << 16, packed.z & 0xFFFF0000u, packed.w << 16, packed.w & 0xFFFF0000u);
-    } else {
-        *reinterpret_cast<uint4 *>(cell + octet_position<BITS>(t, e8) * 16) = packed;
-    }
-    if (e8 == 0) *reinterpret_cast<float4 *>(cell + (XF32 ? 256 : 128)) = meta;
+    uint4 *dst = reinterpret_cast<uint4 *>(cell + octet_position<BITS>(t, e8) * 32);
+    dst[0] = make_uint4(packed.x << 16, packed.x & 0xFFFF0000u, packed.y << 16, packed.y & 0xFFFF0000u);
+    dst[1] = make_uint4(packed.z << 16, packed.z & 0xFFFF0000u, packed.w << 16, packed.w & 0xFFFF0000u);
+    if (e8 == 0) *reinterpret_cast<float4 *>(cell + 256) = meta;
 }
 
 // Steps 1 and 2 for every vector, once per call, for the streamed kernel:
 // cell (v, t) of vector v and subgroup t at out + (v * S_row + t) * cell
 // bytes. Eight threads per subgroup (the grid is a whole number of warps;
 // threads past the end only take part in the shuffles).
-template <int BITS, bool XF32>
+template <int BITS>
 __device__ __forceinline__ void stage_all_body(const uint16_t *x, int K, int S_row, int V, uint8_t *out,
                                                unsigned *counters, int ncounters)
 {
@@ -667,7 +654,7 @@ __device__ __forceinline__ void stage_all_body(const uint16_t *x, int K, int S_r
     uint4 packed;
     float4 meta;
     stage_eight<BITS, false>(raw, packed, meta);
-    if (live) write_cell<BITS, XF32>(out + (size_t(v) * S_row + t) * xs_cell(XF32), t, e8, packed, meta);
+    if (live) write_cell<BITS>(out + (size_t(v) * S_row + t) * kXsF32, t, e8, packed, meta);
 }
 
 // Stages x (one vector) for the one-vector kernel in place: the raw bf16 x of
@@ -1077,7 +1064,7 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CU
 
 // ------------------------------------------------ V vectors: direct loads --
 
-template <int BITS, int GS, int V, bool SBP, bool XF32>
+template <int BITS, int GS, int V, bool SBP>
 __device__ __forceinline__ void qmv_direct_body(const Params &p)
 {
     using T = Traits<BITS, V>;
@@ -1101,7 +1088,7 @@ __device__ __forceinline__ void qmv_direct_body(const Params &p)
     const int nunits = (rb_hi - rb_lo) * cpc_here;  // (row block, chunk) pairs
 
     const int nsub_max = p.cpc * kChunkSubs < p.S_row ? p.cpc * kChunkSubs : p.S_row;
-    const SmemLayout L = smem_layout(BITS, V, nthreads >> 5, nsub_max, p.max_rb, p.cpc, XF32);
+    const SmemLayout L = smem_layout(BITS, V, nthreads >> 5, nsub_max, p.max_rb, p.cpc);
     const uint32_t xs = smem_u32(smem + L.xs);
     float *cvs = reinterpret_cast<float *>(smem + L.cv);
     unsigned *s_next = reinterpret_cast<unsigned *>(smem + L.misc);
@@ -1168,7 +1155,7 @@ __device__ __forceinline__ void qmv_direct_body(const Params &p)
     if (u0 < nunits) load_unit(u0, w_cur, s_cur, b_cur);
     grid_launch_dependents();
     grid_dependency_wait();  // the staged cells are written by the preceding grid
-    constexpr uint32_t kCell = xs_cell(XF32);
+    constexpr uint32_t kCell = kXsF32;
     if (tid == 0) {
         // this CTA's subgroups of every vector: one bulk copy per vector
         mbar_arrive_expect_tx(xbar, uint32_t(V * nsub) * kCell);
@@ -1185,7 +1172,7 @@ __device__ __forceinline__ void qmv_direct_body(const Params &p)
         return;
     }
 
-    const uint32_t xv_bytes = uint32_t(nsub_max) * xs_cell(XF32);
+    const uint32_t xv_bytes = uint32_t(nsub_max) * kXsF32;
     const uint32_t wcell = smem_u32(smem + L.wbuf) + uint32_t(warp) * kRows * T::NP * 512u + uint32_t(lane) * 16u;
     while (u0 < nunits) {
         const Unit g = unit_geo(u0);
@@ -1208,19 +1195,19 @@ __device__ __forceinline__ void qmv_direct_body(const Params &p)
 #pragma unroll
         for (int ps = 0; ps < T::PASSES; ++ps) {
             const int v0 = ps * T::VP;
-            const uint32_t xsub = xs + (uint32_t(v0) * nsub_max + sl) * xs_cell(XF32);
+            const uint32_t xsub = xs + (uint32_t(v0) * nsub_max + sl) * kXsF32;
             uint64_t acc[kRows][T::VP];
             if constexpr (T::PASSES > 1)
-                subgroup_dot_vp_smem<BITS, T::VP, XF32>(wcell, xsub, xv_bytes, acc);
+                subgroup_dot_vp_smem<BITS, T::VP>(wcell, xsub, xv_bytes, acc);
             else
-                subgroup_dot_vp<BITS, T::VP, XF32>(w_cur, xsub, xv_bytes, acc);
+                subgroup_dot_vp<BITS, T::VP>(w_cur, xsub, xv_bytes, acc);
             float val[T::NRED];
 #pragma unroll
             for (int i = 0; i < T::NRED; ++i) val[i] = 0.0f;
 #pragma unroll
             for (int v = 0; v < T::VP; ++v) {
                 if (v0 + v >= V) break;
-                const float4 meta = lds_f4(xsub + v * xv_bytes + (XF32 ? 256 : 128));
+                const float4 meta = lds_f4(xsub + v * xv_bytes + 256);
 #pragma unroll
                 for (int r = 0; r < kRows; ++r) {
                     const float term = subgroup_term<true>(pair_lo(acc[r][v]), pair_hi(acc[r][v]), fs[r], fb[r], meta.x, meta.y, meta.z);
@@ -1262,20 +1249,19 @@ __global__ void __launch_bounds__(kThreadsV1, 1)
     qmv_ring_body<BITS, GS, SBP>(&map_w, &map_s, &map_b, p);
 }
 
-// XF32: x' staged as fp32 (else bf16).
-template <int BITS, int GS, int V, bool SBP, bool XF32>
+template <int BITS, int GS, int V, bool SBP>
 __global__ void __launch_bounds__(kThreadsVN, 1) qmv_streamed(const Params p)
 {
-    qmv_direct_body<BITS, GS, V, SBP, XF32>(p);
+    qmv_direct_body<BITS, GS, V, SBP>(p);
 }
 
 // The streamed kernel's x staging, once per call (kStageThreads a block).
 constexpr int kStageThreads = 128;
-template <int BITS, bool XF32>
+template <int BITS>
 __global__ void __launch_bounds__(kStageThreads)
     qmv_stage_x(const uint16_t *x, int K, int S_row, int V, uint8_t *out, unsigned *counters, int ncounters)
 {
-    stage_all_body<BITS, XF32>(x, K, S_row, V, out, counters, ncounters);
+    stage_all_body<BITS>(x, K, S_row, V, out, counters, ncounters);
 }
 
 }  // namespace qmv

@@ -51,30 +51,25 @@ cudaError_t launch_m1(const RingMaps &maps, const RingParams &p, const Launch &l
 template <int BITS, int GS, int V>
 cudaError_t launch_v(const Params &p, const Launch &l, cudaStream_t stream)
 {
-    static int configured[4][64] = {};
-    if (p.sb_packed) {
-        if (p.xf32) return launch_one(qmv_streamed<BITS, GS, V, true, true>, configured[3], l, stream, p);
-        return launch_one(qmv_streamed<BITS, GS, V, true, false>, configured[2], l, stream, p);
-    }
-    if (p.xf32) return launch_one(qmv_streamed<BITS, GS, V, false, true>, configured[1], l, stream, p);
-    return launch_one(qmv_streamed<BITS, GS, V, false, false>, configured[0], l, stream, p);
+    static int configured[2][64] = {};
+    if (p.sb_packed) return launch_one(qmv_streamed<BITS, GS, V, true>, configured[1], l, stream, p);
+    return launch_one(qmv_streamed<BITS, GS, V, false>, configured[0], l, stream, p);
 }
 
 // The call's x staging for the streamed kernel (one thread per eight
 // elements of a vector).
 template <int BITS>
-cudaError_t launch_stage(bool xf32, const uint16_t *x, int K, int S_row, int V, uint8_t *out, unsigned *counters,
-                         int ncounters, bool pdl, cudaStream_t stream)
+cudaError_t launch_stage(const uint16_t *x, int K, int S_row, int V, uint8_t *out, unsigned *counters, int ncounters,
+                         bool pdl, cudaStream_t stream)
 {
-    static int configured[2][64] = {};
+    static int configured[64] = {};
     const long long threads = (long long)V * S_row * 8;
     Launch l;
     l.grid = dim3(unsigned((threads + kStageThreads - 1) / kStageThreads));
     l.threads = kStageThreads;
     l.smem = 0;
     l.pdl = pdl;
-    if (xf32) return launch_one(qmv_stage_x<BITS, true>, configured[1], l, stream, x, K, S_row, V, out, counters, ncounters);
-    return launch_one(qmv_stage_x<BITS, false>, configured[0], l, stream, x, K, S_row, V, out, counters, ncounters);
+    return launch_one(qmv_stage_x<BITS>, configured, l, stream, x, K, S_row, V, out, counters, ncounters);
 }
 
 template <int BITS, int GS>

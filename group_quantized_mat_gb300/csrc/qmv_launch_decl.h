@@ -29,8 +29,8 @@ struct Launch {
 #define QMV_DECLARE_LAUNCH(name)                                                                                  \
     cudaError_t name##_m1(const RingMaps &maps, const RingParams &p, const Launch &l, cudaStream_t stream);      \
     cudaError_t name##_streamed(int V, const Params &p, const Launch &l, cudaStream_t stream);                   \
-    cudaError_t name##_stage(bool xf32, const uint16_t *x, int K, int S_row, int V, uint8_t *out,                \
-                             unsigned *counters, int ncounters, bool pdl, cudaStream_t stream);
+    cudaError_t name##_stage(const uint16_t *x, int K, int S_row, int V, uint8_t *out, unsigned *counters,       \
+                             int ncounters, bool pdl, cudaStream_t stream);
 QMV_DECLARE_LAUNCH(launch_b4g64)
 QMV_DECLARE_LAUNCH(launch_b4g128)
 QMV_DECLARE_LAUNCH(launch_b2g64)

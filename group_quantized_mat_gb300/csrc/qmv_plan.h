@@ -17,10 +17,7 @@ constexpr int kChunkElems = kSub * kChunkSubs;
 constexpr int kRows = 4;            // rows per work unit; every lane of the warp works on all of them
 constexpr int kMaxM = 16;
 constexpr int kXsB16 = 144;         // bytes per staged subgroup, one-vector kernel: 128 B of bf16 x'' + 16 B of (sx, f1, f2, 0)
-constexpr int kXsF32 = 272;         // bytes per staged subgroup and vector, streamed kernel, fp32 x': 256 B + (sx, f1, f2, 0)
-// Staged bytes per subgroup and vector of the streamed kernel: fp32 x' (no
-// unpacking in the datapath) or bf16 x' (half the shared memory).
-__host__ __device__ constexpr int xs_cell(bool xf32) { return xf32 ? kXsF32 : kXsB16; }
+constexpr int kXsF32 = 272;         // bytes per staged subgroup and vector, streamed kernel: 256 B of fp32 x' + (sx, f1, f2, 0)
 
 __host__ __device__ constexpr int sub_bytes(int bits) { return kSub * bits / 8; }
 __host__ __device__ constexpr int chunk_bytes(int bits) { return kChunkElems * bits / 8; }
@@ -53,7 +50,6 @@ struct Params {
     int cpc;                  // chunks per CTA
     int max_rb;               // row blocks of the largest CTA share
     int f32_out;
-    int xf32;                 // streamed kernel: x' staged as fp32 (else bf16)
     const uint8_t *xs_staged; // streamed kernel: the call's staged cells [V][S_row] (qmv_stage_x)
     int sb_packed;            // 1: scales is the interleaved uint32 array (scale low, bias high), biases unused
 };
@@ -88,11 +84,11 @@ struct SmemLayout {
     int xs, cv, wbuf, misc, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int bits, int V, int warps, int nsub, int max_rb, int cpc, bool xf32)
+__host__ __device__ inline SmemLayout smem_layout(int bits, int V, int warps, int nsub, int max_rb, int cpc)
 {
     SmemLayout L;
     L.xs = 0;
-    L.cv = align_up(V * nsub * xs_cell(xf32), 16);
+    L.cv = align_up(V * nsub * kXsF32, 16);
     L.wbuf = align_up(L.cv + max_rb * kRows * cpc * V * 4, 16);
     L.misc = L.wbuf + (vectors_per_pass(V) < V ? warps * kRows * 32 * sub_bytes(bits) : 0);
     L.total = L.misc + 16 + 128;  // next-unit counter and the x barrier; slack for aligning the dynamic base

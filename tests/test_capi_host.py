@@ -103,13 +103,15 @@ def test_split_plan(lib):
     assert g.qmv_workspace_size(1, 256, 1024, 4, 64) == 0
     assert g.qmv_workspace_size(1, 15360, 3840, 4, 64) == 0
     assert g.qmv_workspace_size(1, 3840, 15360, 4, 64) == 0
-    # M >= 2: the call's staged x cells [M][K/64] (144 bytes with bf16 x',
-    # 272 with fp32 x'). On K = 3840 bf16 cells let a CTA take all of K, so
-    # there is no K split; fp32 cells would have forced one.
-    assert g.qmv_workspace_size(13, 15360, 3840, 4, 64) == a256(13 * 60 * 144)
-    assert g.qmv_workspace_size(16, 15360, 3840, 4, 64) == a256(16 * 60 * 144)
+    # M >= 2: the call's staged x cells [M][K/64], 272 bytes each (fp32 x'
+    # and the subgroup's meta). On K = 3840 the cells of all of K fit a CTA's
+    # shared memory up to M = 10; from M = 11 CTAs split K in two.
     assert g.qmv_workspace_size(2, 15360, 3840, 4, 64) == a256(2 * 60 * 272)
-    # K = 15360 splits either way, so fp32 cells; chunk values meet in the
+    assert g.qmv_workspace_size(10, 15360, 3840, 4, 64) == a256(10 * 60 * 272)
+    split_p = lambda M: a256(3840 * 4) + 2 * M * 15360 * 4
+    assert g.qmv_workspace_size(11, 15360, 3840, 4, 64) == a256(split_p(11)) + a256(11 * 60 * 272)
+    assert g.qmv_workspace_size(13, 15360, 3840, 4, 64) == a256(split_p(13)) + a256(13 * 60 * 272)
+    # K = 15360 splits; chunk values meet in the
     # workspace first: a 256-byte-aligned block of one counter per 4-row
     # block, then ks x M x N fp32 partials, then the cells
     split13 = (960 * 4 + 255) // 256 * 256 + 8 * 13 * 3840 * 4
@@ -119,7 +121,7 @@ def test_split_plan(lib):
     assert w16 == a256(split13 + 8 * 3 * 3840 * 4) + a256(16 * 240 * 272)
     # M above 16 runs as launches of 16 vectors and one of the remainder: the
     # widest of those decides
-    assert g.qmv_workspace_size(17, 15360, 3840, 4, 64) == a256(16 * 60 * 144)
+    assert g.qmv_workspace_size(17, 15360, 3840, 4, 64) == a256(split_p(16)) + a256(16 * 60 * 272)
     assert g.qmv_workspace_size(20, 3840, 15360, 4, 64) == w16
     assert g.qmv_workspace_size(33, 3840, 15360, 4, 64) == w16
     assert g.qmv_workspace_size(256, 3840, 15360, 4, 64) == w16
