@@ -179,6 +179,31 @@ def test_interleaved_metadata_gives_identical_results(N, K, bits, gs):
         assert np.array_equal(y.cpu().numpy().view(np.uint32), want.view(np.uint32)), f"M={M}"
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 15360, 3840), (4, 2048, 3840), (13, 3840, 15360), (20, 1000, 5120)])
+def test_pdl_launches_wait_for_the_producer_of_x(M, N, K):
+    """With QMV_PDL a launch may start while the preceding kernel runs; x is
+    written by exactly such a kernel here, so reading it before the
+    dependency wait would give other results than the plain launch."""
+    inp = synth.make_inputs(N, K, M, 4, 64, seed=70 + M)
+    dp = DeviceProblem(inp)
+    rng = np.random.default_rng(M)
+    xs = [dp.x[rng.permutation(M)].contiguous() for _ in range(4)]
+    want = [dp.run(x=x, flags=g.F32_OUT) for x in xs]
+    x_buf = torch.empty_like(dp.x)
+    s = torch.cuda.Stream()
+    outs = []
+    with torch.cuda.stream(s):
+        for x in xs:
+            y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+            x_buf.zero_()
+            x_buf.copy_(x)  # the kernel right before the call writes x
+            g.qmv_run_ex(dp.w, dp.s, dp.b, x_buf, y, M, N, K, 4, 64, flags=g.F32_OUT | g.PDL, stream=s)
+            outs.append(y)
+    torch.cuda.synchronize()
+    for got, ref in zip(outs, want):
+        assert np.array_equal(got.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
 def test_position_invariance():
     inp = synth.make_inputs(3840, 3840, 13, 4, 64, seed=11)
     dp = DeviceProblem(inp)
