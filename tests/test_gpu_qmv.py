@@ -204,6 +204,46 @@ def test_pdl_launches_wait_for_the_producer_of_x(M, N, K):
         assert np.array_equal(got.cpu().numpy().view(np.uint32), ref.view(np.uint32))
 
 
+@pytest.mark.parametrize("case", ["x_zero", "s_zero", "q_zero", "q_max"])
+def test_degenerate_inputs(o, case):
+    """The method's degenerate cases: zero activations (y = 0), zero scales
+    (bias terms only), all-zero and all-maximum fields. Parity with the
+    oracle, and streamed columns equal to M = 1 bit for bit."""
+    N, K = 260, 5120
+    inp = synth.make_inputs(N, K, 4, 4, 64, seed=81)
+    if case == "x_zero":
+        inp.x = np.zeros_like(inp.x)
+    elif case == "s_zero":
+        inp.scales = np.zeros_like(inp.scales)
+    elif case == "q_zero":
+        inp.q = np.zeros_like(inp.q)
+    else:
+        inp.q = np.full_like(inp.q, 15)
+    dp = DeviceProblem(inp)
+    y = dp.run(flags=g.F32_OUT)
+    singles = np.stack([dp.run(x=dp.x[m:m + 1].contiguous(), M=1, flags=g.F32_OUT)[0] for m in range(4)])
+    assert np.array_equal(y.view(np.uint32), singles.view(np.uint32))
+    ref, terms = oracle_rows(o, inp)
+    check_parity(dp.run(), ref, terms, case)
+    if case == "x_zero":
+        assert np.all(y == 0.0)
+
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_long_rows(o, M):
+    """K = 2^22: thousands of chunks per row, hundreds of K-ranges meeting in
+    the workspace."""
+    N, K = 5, 1 << 22
+    inp = synth.make_inputs(N, K, M, 4, 64, seed=90 + M)
+    dp = DeviceProblem(inp)
+    y = dp.run(flags=g.F32_OUT)
+    if M > 1:
+        singles = np.stack([dp.run(x=dp.x[m:m + 1].contiguous(), M=1, flags=g.F32_OUT)[0] for m in range(M)])
+        assert np.array_equal(y.view(np.uint32), singles.view(np.uint32))
+    ref, terms = oracle_rows(o, inp)
+    check_parity(dp.run(), ref, terms, f"K=2^22 M={M}")
+
+
 def test_position_invariance():
     inp = synth.make_inputs(3840, 3840, 13, 4, 64, seed=11)
     dp = DeviceProblem(inp)
