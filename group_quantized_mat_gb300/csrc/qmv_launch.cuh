@@ -3,6 +3,8 @@
 // compile in parallel.
 #pragma once
 
+#include <atomic>
+
 #include "qmv_kernel.cuh"
 #include "qmv_launch_decl.h"
 
@@ -12,18 +14,24 @@ static_assert(kConsumersV1 == kRingConsumers && kProducersV1 == kRingProducers, 
 static_assert(kThreadsVN == kStreamedWarps * 32, "launch bounds");
 
 template <typename Kern, typename... Args>
-cudaError_t launch_one(Kern kern, int (&configured)[64], const Launch &l, cudaStream_t stream, Args... args)
+cudaError_t launch_one(Kern kern, std::atomic<int> (&configured)[64], const Launch &l, cudaStream_t stream, Args... args)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 64) return cudaErrorInvalidDevice;
-    // The opt-in dynamic shared-memory limit is a per-device kernel attribute;
-    // raise it when this launch needs more than it was last set to.
-    if (configured[dev] < int(l.smem)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(l.smem));
+    // The opt-in dynamic shared-memory limit is a per-device kernel attribute.
+    // The first launch that needs more than the default sets it to the
+    // device's maximum, the same value whichever host thread gets there
+    // first, so concurrent callers never lower it under each other.
+    if (configured[dev].load() < int(l.smem)) {
+        int most = 0;
+        e = cudaDeviceGetAttribute(&most, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         if (e != cudaSuccess) return e;
-        configured[dev] = int(l.smem);
+        const int limit = most > int(l.smem) ? most : int(l.smem);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
+        if (e != cudaSuccess) return e;
+        configured[dev].store(limit);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = l.grid;
@@ -43,7 +51,7 @@ cudaError_t launch_one(Kern kern, int (&configured)[64], const Launch &l, cudaSt
 template <int BITS, int GS>
 cudaError_t launch_m1(const RingMaps &maps, const RingParams &p, const Launch &l, cudaStream_t stream)
 {
-    static int configured[2][64] = {};
+    static std::atomic<int> configured[2][64] = {};
     if (p.sb_packed) return launch_one(qmv_m1<BITS, GS, true>, configured[1], l, stream, maps.w, maps.s, maps.b, p);
     return launch_one(qmv_m1<BITS, GS, false>, configured[0], l, stream, maps.w, maps.s, maps.b, p);
 }
@@ -51,7 +59,7 @@ cudaError_t launch_m1(const RingMaps &maps, const RingParams &p, const Launch &l
 template <int BITS, int GS, int V>
 cudaError_t launch_v(const Params &p, const Launch &l, cudaStream_t stream)
 {
-    static int configured[2][64] = {};
+    static std::atomic<int> configured[2][64] = {};
     if (p.sb_packed) return launch_one(qmv_streamed<BITS, GS, V, true>, configured[1], l, stream, p);
     return launch_one(qmv_streamed<BITS, GS, V, false>, configured[0], l, stream, p);
 }
@@ -62,7 +70,7 @@ template <int BITS>
 cudaError_t launch_stage(const uint16_t *x, int K, int S_row, int V, uint8_t *out, unsigned *counters, int ncounters,
                          bool pdl, cudaStream_t stream)
 {
-    static int configured[64] = {};
+    static std::atomic<int> configured[64] = {};
     const long long threads = (long long)V * S_row * 8;
     Launch l;
     l.grid = dim3(unsigned((threads + kStageThreads - 1) / kStageThreads));
