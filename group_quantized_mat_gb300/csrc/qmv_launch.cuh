@@ -4,6 +4,7 @@
 #pragma once
 
 #include <atomic>
+#include <mutex>
 
 #include "qmv_kernel.cuh"
 #include "qmv_launch_decl.h"
@@ -20,18 +21,18 @@ cudaError_t launch_one(Kern kern, std::atomic<int> (&configured)[64], const Laun
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 64) return cudaErrorInvalidDevice;
-    // The opt-in dynamic shared-memory limit is a per-device kernel attribute.
-    // The first launch that needs more than the default sets it to the
-    // device's maximum, the same value whichever host thread gets there
-    // first, so concurrent callers never lower it under each other.
+    // The opt-in dynamic shared-memory limit is a per-device kernel attribute;
+    // raise it when this launch needs more than it was last set to. Raising
+    // happens under a lock, so concurrent host threads never lower it under
+    // each other; the cached value is stored only after the attribute is set.
     if (configured[dev].load() < int(l.smem)) {
-        int most = 0;
-        e = cudaDeviceGetAttribute(&most, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e != cudaSuccess) return e;
-        const int limit = most > int(l.smem) ? most : int(l.smem);
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
-        if (e != cudaSuccess) return e;
-        configured[dev].store(limit);
+        static std::mutex m;
+        std::lock_guard<std::mutex> lock(m);
+        if (configured[dev].load() < int(l.smem)) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(l.smem));
+            if (e != cudaSuccess) return e;
+            configured[dev].store(int(l.smem));
+        }
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = l.grid;
