@@ -29,9 +29,9 @@
 //  5. one rounding to bf16, nearest even.
 // Field readings (both give the products of step 1 bit for bit):
 //  * qmv_streamed: x'_i = x_i * 2^(254 - bits*k_i - E), k_i = position of
-//    element i inside its 16-bit half word, staged as bf16; field q_i is the
-//    fp32 whose bit pattern is q_i << (bits*k_i), the subnormal
-//    q_i * 2^(bits*k_i - 149); one fma.rn.f32x2 per element pair.
+//    element i inside its 16-bit half word, exactly a bf16 value, staged as
+//    fp32; field q_i is the fp32 whose bit pattern is q_i << (bits*k_i), the
+//    subnormal q_i * 2^(bits*k_i - 149); one fma.rn.f32x2 per element pair.
 //  * qmv_m1: x''_i = x_i * 2^(238 - bits*j_i - E), j_i = position of the
 //    field inside its byte, staged as bf16; field q_i is the bf16 half whose
 //    bit pattern is q_i << (bits*j_i), i.e. q_i * 2^(bits*j_i - 133) (the low
@@ -49,13 +49,16 @@
 // some chunks; lane l of the warp processing a unit owns subgroup l of each
 // of its chunks in all 4 rows. Warps take units from a shared counter.
 //  * qmv_m1 (one vector): producer warps stream units (4 whole rows in one
-//    1-D bulk copy when they fit, else the rows' chunks, plus 1-D tensor-map
-//    boxes of the rows' scales and biases) into a CTA-wide ring of
-//    shared-memory slots, one "full" and one "empty" mbarrier per slot;
-//    consumer warps compute them.
-//  * qmv_streamed (V vectors): a warp loads its unit's bytes (the lane's own
-//    subgroup of 4 rows of one chunk), scales and biases straight into
-//    registers; V times the arithmetic hides the latency.
+//    1-D bulk copy when they fit, else 4 rows x some chunks as one 2-D
+//    tensor-map tile or one copy per row, plus tensor-map boxes of the rows'
+//    scales and biases) into a CTA-wide ring of shared-memory slots, one
+//    "full" and one "empty" mbarrier per slot; consumer warps compute them.
+//    The CTA's x arrives by one bulk copy and is staged in place.
+//  * qmv_streamed (V vectors): qmv_stage_x stages every vector's x' once per
+//    call into the workspace; the CTA brings in its range with one bulk copy
+//    per vector. A warp loads its unit's bytes (the lane's own subgroup of 4
+//    rows of one chunk), scales and biases straight into registers; V times
+//    the arithmetic hides the latency.
 #pragma once
 
 #include <cuda.h>
