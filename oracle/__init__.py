@@ -1,4 +1,4 @@
-"""CPU oracle for the affine group-quantized mat-vec (qmv) -- TEST INFRASTRUCTURE.
+"""CPU oracle for the group-quantized mat-vec (qmv; affine and mxfp4) -- TEST INFRASTRUCTURE.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
 reference leg may import this package. The product path never does.
@@ -75,6 +75,14 @@ def _load(mutant: int = 0) -> ctypes.CDLL:
             f.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I]
         lib.oracle_qmv_f32_factored.restype = _I
         lib.oracle_qmv_f32_factored.argtypes = [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I]
+        lib.oracle_e2m1_to_f64.restype = ctypes.c_double
+        lib.oracle_e2m1_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_e8m0_to_f64.restype = ctypes.c_double
+        lib.oracle_e8m0_to_f64.argtypes = [ctypes.c_uint8]
+        for fn in ("oracle_mxfp4_qmv_f64", "oracle_mxfp4_abs_terms"):
+            f = getattr(lib, fn)
+            f.restype = None
+            f.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64]
         lib.oracle_mutant.restype = _I
         _libs[mutant] = lib
         return lib
@@ -162,6 +170,33 @@ class Oracle:
         used = self.lib.oracle_qmv_f32_factored(_ptr(wq), _ptr(s), _ptr(b), _ptr(x), _ptr(y),
                                                 _ptr(y32), M, N, K, bits, gs, int(nthreads))
         return y, y32, used
+
+    # -- mxfp4 (E2M1 elements, one E8M0 scale per 32 along K) --------------
+    def e2m1_to_f64(self, codes) -> np.ndarray:
+        return np.array([self.lib.oracle_e2m1_to_f64(int(c)) for c in np.ravel(codes)],
+                        dtype=np.float64).reshape(np.shape(codes))
+
+    def e8m0_to_f64(self, codes) -> np.ndarray:
+        return np.array([self.lib.oracle_e8m0_to_f64(int(c)) for c in np.ravel(codes)],
+                        dtype=np.float64).reshape(np.shape(codes))
+
+    def _mx(self, fn, wq, scales, x):
+        wq = np.ascontiguousarray(wq, dtype=np.uint32)
+        scales = np.ascontiguousarray(scales, dtype=np.uint8)
+        x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.uint16)
+        N = wq.shape[0]
+        M, K = x.shape
+        assert K % 32 == 0 and wq.shape[1] == K // 8 and scales.shape == (N, K // 32)
+        y = np.empty((M, N), dtype=np.float64)
+        getattr(self.lib, fn)(_ptr(wq), _ptr(scales), _ptr(x), _ptr(y), M, N, K)
+        return y
+
+    def mxfp4_qmv_f64(self, wq, scales, x):
+        """y[M, N] = sum_i scale * e2m1(q) * x, fp64 (wq from ``pack(codes, 4)``)."""
+        return self._mx("oracle_mxfp4_qmv_f64", wq, scales, x)
+
+    def mxfp4_abs_terms(self, wq, scales, x):
+        return self._mx("oracle_mxfp4_abs_terms", wq, scales, x)
 
 
 def tolerance_ok(y_test: np.ndarray, y_ref: np.ndarray, abs_terms: np.ndarray,

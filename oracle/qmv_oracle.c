@@ -307,3 +307,93 @@ int oracle_qmv_f32_factored(const uint32_t *wq, const uint16_t *scales, const ui
     free(jobs);
     return used;
 }
+
+/* ------------------------------------------------ mxfp4 (the fp mode) -- */
+
+/*
+ * The pages name a second phase, an order-preserving streamed qmv for the
+ * fp quantization modes ("mxfp4", mlxcel issue #1289, section "Scope
+ * limits, stated honestly"), without giving the format. The plain reading taken here is the
+ * OCP Microscaling (MX) v1.0 MXFP4 format:
+ *
+ *   element  E2M1, 4 bits: sign (bit 3), exponent (bits 2..1, bias 1),
+ *            mantissa (bit 0); exponent field 0 is subnormal (no implicit 1).
+ *   scale    E8M0, one unsigned byte per block of 32 consecutive elements
+ *            along K: 2^(e - 127); e = 255 is NaN.
+ *
+ *   w[n, i] = scale[n, i/32] * e2m1(q[n, i])
+ *   y[m, n] = sum_i w[n, i] * x[m, i]
+ *
+ * The 4-bit codes use the same packed layout as the affine 4-bit fields
+ * (field j of a word at bits [4j, 4j+4)).
+ */
+
+double oracle_e2m1_to_f64(uint8_t code)
+{
+    int sign = (code >> 3) & 1;
+    int e = (code >> 1) & 3;
+    int m = code & 1;
+#if ORACLE_MUTANT == 8 /* mistake: sign bit ignored */
+    sign = 0;
+#endif
+    double mag;
+#if ORACLE_MUTANT == 9 /* mistake: exponent field 0 read as a normal number */
+    mag = ldexp(1.0 + 0.5 * m, e - 1);
+#else
+    if (e == 0)
+        mag = 0.5 * m; /* subnormal: (m / 2) * 2^(1 - bias) */
+    else
+        mag = ldexp(1.0 + 0.5 * m, e - 1); /* (1 + m / 2) * 2^(e - bias) */
+#endif
+    return sign ? -mag : mag;
+}
+
+double oracle_e8m0_to_f64(uint8_t e)
+{
+    if (e == 255)
+        return NAN;
+    int bias = 127;
+#if ORACLE_MUTANT == 10 /* mistake: exponent bias off by one */
+    bias = 128;
+#endif
+    return ldexp(1.0, (int)e - bias);
+}
+
+static double mx_weight_f64(const uint32_t *row_words, const uint8_t *s_row, int64_t i, int64_t B)
+{
+    int64_t blk = i / 32;
+#if ORACLE_MUTANT == 11 /* mistake: neighbouring blocks' scales exchanged */
+    if ((blk ^ 1) < B)
+        blk ^= 1;
+#endif
+    (void)B;
+    return oracle_e8m0_to_f64(s_row[blk]) * oracle_e2m1_to_f64((uint8_t)oracle_field(row_words, i, 4));
+}
+
+/* y[m, n] = sum_i (scale * e2m1(q)) x: dequantize, then dot, in fp64. */
+void oracle_mxfp4_qmv_f64(const uint32_t *wq, const uint8_t *scales, const uint16_t *x, double *y,
+                          int64_t M, int64_t N, int64_t K)
+{
+    int64_t wpr = K / 8, B = K / 32;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t i = 0; i < K; ++i)
+                acc += mx_weight_f64(wq + n * wpr, scales + n * B, i, B) * oracle_bf16_to_f64(x[m * K + i]);
+            y[m * N + n] = acc;
+        }
+}
+
+/* T[m, n] = sum_i |w_i x_i| in fp64, the scale of the acceptance bound. */
+void oracle_mxfp4_abs_terms(const uint32_t *wq, const uint8_t *scales, const uint16_t *x, double *t,
+                            int64_t M, int64_t N, int64_t K)
+{
+    int64_t wpr = K / 8, B = K / 32;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t i = 0; i < K; ++i)
+                acc += fabs(mx_weight_f64(wq + n * wpr, scales + n * B, i, B) * oracle_bf16_to_f64(x[m * K + i]));
+            t[m * N + n] = acc;
+        }
+}

@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for affine group-quantized mat-vec (qmv).
+"""Seeded synthetic inputs for group-quantized mat-vec (qmv): affine and mxfp4.
 
 This module only draws random numbers. It holds none of the method's
 arithmetic (no packing, no extraction, no dot products), so both the CUDA
@@ -76,6 +76,37 @@ def make_inputs(N: int, K: int, M: int, bits: int = 4, group_size: int = 64, see
     return QmvInputs(QmvProblem(N, K, M, bits, group_size, seed), q, s, b, x)
 
 
+@dataclass
+class MxInputs:
+    N: int
+    K: int
+    M: int
+    seed: int
+    codes: np.ndarray    # uint8  [N, K]      E2M1 codes, 0 .. 15
+    scales: np.ndarray   # uint8  [N, K // 32] E8M0 exponent bytes
+    x: np.ndarray        # uint16 [M, K]      bf16 bit patterns
+
+
+def make_mxfp4_inputs(N: int, K: int, M: int, seed: int = 0, scale_lo: int = 118, scale_hi: int = 122) -> MxInputs:
+    """Seeded inputs of the mxfp4 mode (E2M1 codes, one E8M0 byte per 32 along K).
+
+    * ``codes``  uniform over all 16 E2M1 codes (both zeros, both signs, up to +-6)
+    * ``scales`` uniform integer exponent bytes in [scale_lo, scale_hi] (2^-9 .. 2^-5
+      by default: weights up to about 0.19 in magnitude, as for a checkpoint's
+      projection matrices)
+    * ``x``      N(0, 1) rounded to bf16
+
+    Draw order: codes, scales, x, from one ``torch.Generator(device="cpu")``.
+    """
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    codes = torch.randint(0, 16, (N, K), generator=g, dtype=torch.uint8)
+    scales = torch.randint(scale_lo, scale_hi + 1, (N, K // 32), generator=g, dtype=torch.int32).to(torch.uint8)
+    x = make_activations(M, K, seed, generator=g)
+    return MxInputs(N, K, M, seed, codes.numpy().copy(), scales.numpy().copy(), x)
+
+
 def bf16_bits_to_f32(a: np.ndarray) -> np.ndarray:
     """Widen bf16 bit patterns to fp32 (exact: bf16 is the top half of binary32)."""
     return (a.astype(np.uint32) << 16).view(np.float32)
@@ -97,4 +128,10 @@ WORKLOADS = {
     # 2-bit variant of the projection
     "proj_15360x3840_2b_g64": dict(N=15360, K=3840, bits=2, group_size=64, Ms=(1, 13)),
     "proj_15360x3840_2b_g128": dict(N=15360, K=3840, bits=2, group_size=128, Ms=(1, 13)),
+}
+
+# The same shapes in the mxfp4 mode (E2M1 codes, 32-element E8M0 blocks).
+MX_WORKLOADS = {
+    "proj_15360x3840_mxfp4": dict(N=15360, K=3840, Ms=(1, 13)),
+    "down_3840x15360_mxfp4": dict(N=3840, K=15360, Ms=(1, 13)),
 }

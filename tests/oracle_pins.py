@@ -3,8 +3,9 @@
 Each pin takes an ``oracle.Oracle`` and returns ``(ok, detail)``. The pins use
 library routines (torch's bf16 rounding, numpy's float64 matmul), exact
 rational arithmetic (``fractions.Fraction``), closed forms of special cases,
-the float-floor field chain of llama.cpp PR #159 "How", and hand-worked
-fixtures of the field order (``tests/golden/field_order.txt``).
+the float-floor field chain of llama.cpp PR #159 "How", hand-worked
+fixtures of the field order (``tests/golden/field_order.txt``) and, for the
+mxfp4 mode, ml_dtypes' E2M1 and torch's E8M0 decoders.
 
 ``test_oracle.py`` asserts every pin passes on the real oracle, and that every
 oracle build with a planted mistake (``-DORACLE_MUTANT=k``) fails at least one.
@@ -271,6 +272,118 @@ def pin_f32_form(o):
     return True, "fp32 factored form within 1e-5*sum|wx| of fp64; bf16 output = RNE(fp32)"
 
 
+# ----------------------------------------------------------------- mxfp4 --
+# The fp mode: E2M1 codes, one E8M0 scale byte per 32 elements along K (the
+# OCP MX v1.0 MXFP4 format, the reading taken for the pages' "mxfp4").
+_MX_SHAPES = [(5, 32, 1), (6, 96, 2), (3, 256, 3), (4, 1024, 1)]
+
+
+def _mx_decode_numpy(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """Dense fp64 weights through library decoders: ml_dtypes' float4_e2m1fn for
+    the elements, torch's float8_e8m0fnu for the block scales."""
+    import pytest
+    ml_dtypes = pytest.importorskip("ml_dtypes")
+    v = np.ascontiguousarray(codes, dtype=np.uint8).view(ml_dtypes.float4_e2m1fn).astype(np.float64)
+    sc = torch.from_numpy(np.ascontiguousarray(scales, dtype=np.uint8)).view(torch.float8_e8m0fnu)
+    sc = sc.to(torch.float64).numpy()
+    return v * np.repeat(sc, 32, axis=1)
+
+
+def pin_mx_e2m1_value_set(o):
+    """What the E2M1 layout fixes without any table: +0 at code 0, -0 at code 8,
+    the sign bit negates exactly, magnitudes rise strictly with the code, the
+    subnormal code 1 is half the smallest normal code 2, and each normal binade
+    holds two values, the upper one 1.5 times the lower."""
+    v = o.e2m1_to_f64(np.arange(16))
+    if v[0] != 0.0 or np.signbit(v[0]) or v[8] != 0.0 or not np.signbit(v[8]):
+        return False, f"zeros: {v[0]!r}, {v[8]!r}"
+    if not np.array_equal(v[8:], -v[:8]):
+        return False, f"sign bit does not negate: {v.tolist()}"
+    if not np.all(np.diff(v[:8]) > 0):
+        return False, f"magnitudes not increasing: {v[:8].tolist()}"
+    if v[1] * 2 != v[2]:
+        return False, f"subnormal {v[1]} is not half the smallest normal {v[2]}"
+    for e in (1, 2, 3):
+        lo, hi = v[2 * e], v[2 * e + 1]
+        if hi != 1.5 * lo or (e > 1 and lo != 2 * v[2 * e - 2]):
+            return False, f"binade {e}: {lo}, {hi}"
+    return True, "E2M1 value set has the layout's structure"
+
+
+def pin_mx_e2m1_vs_ml_dtypes(o):
+    import pytest
+    ml_dtypes = pytest.importorskip("ml_dtypes")
+    ours = o.e2m1_to_f64(np.arange(16))
+    ref = np.arange(16, dtype=np.uint8).view(ml_dtypes.float4_e2m1fn).astype(np.float64)
+    same = np.array_equal(ours, ref) and np.array_equal(np.signbit(ours), np.signbit(ref))
+    return same, f"oracle {ours.tolist()} vs ml_dtypes {ref.tolist()}"
+
+
+def pin_mx_e8m0_vs_torch(o):
+    ours = o.e8m0_to_f64(np.arange(256))
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    same = np.array_equal(ours, ref, equal_nan=True) and np.isnan(ours[255])
+    bad = np.nonzero(~((ours == ref) | (np.isnan(ours) & np.isnan(ref))))[0]
+    return bool(same), f"{bad.size} of 256 scale bytes differ from torch float8_e8m0fnu (first {bad[:4].tolist()})"
+
+
+def pin_mx_dequant_vs_numpy(o):
+    for N, K, M in _MX_SHAPES:
+        inp = synth.make_mxfp4_inputs(N, K, M, seed=5)
+        w = o.pack(inp.codes, 4)
+        y = o.mxfp4_qmv_f64(w, inp.scales, inp.x)
+        T = o.mxfp4_abs_terms(w, inp.scales, inp.x)
+        W = _mx_decode_numpy(inp.codes, inp.scales)
+        ref = _f64(inp.x) @ W.T
+        tref = np.abs(_f64(inp.x)) @ np.abs(W).T
+        if not np.all(np.abs(y - ref) <= 1e-12 * tref + 1e-300):
+            return False, f"mxfp4 dequant vs numpy {(N, K, M)}: max {np.max(np.abs(y - ref))}"
+        if not np.allclose(T, tref, rtol=1e-12, atol=0):
+            return False, f"mxfp4 abs terms vs numpy {(N, K, M)}"
+    return True, "mxfp4 fp64 dequantize-then-dot agrees with numpy over library-decoded weights"
+
+
+def pin_mx_closed_forms(o):
+    import math
+    N, K = 3, 128
+    x = synth.make_mxfp4_inputs(1, K, 2, seed=6).x
+    xf = _f64(x)
+    ones = np.full((N, K), 0b0010, dtype=np.uint8)      # E2M1 +1.0
+    unit = np.full((N, K // 32), 127, dtype=np.uint8)   # E8M0 2^0
+    y = o.mxfp4_qmv_f64(o.pack(ones, 4), unit, x)
+    for m in range(2):
+        if not np.all(y[m] == math.fsum(xf[m].tolist())):
+            return False, "codes +1.0 with unit scales must give sum(x)"
+    zeros = np.where(np.arange(K) % 2 == 0, 0, 8).astype(np.uint8)[None].repeat(N, 0)
+    if np.any(o.mxfp4_qmv_f64(o.pack(zeros, 4), unit, x) != 0.0):
+        return False, "codes +-0 must give 0"
+    inp = synth.make_mxfp4_inputs(N, K, 2, seed=7)
+    w = o.pack(inp.codes, 4)
+    y0 = o.mxfp4_qmv_f64(w, inp.scales, inp.x)
+    # flipping every sign bit negates y exactly
+    if not np.array_equal(o.mxfp4_qmv_f64(o.pack(inp.codes ^ 8, 4), inp.scales, inp.x), -y0):
+        return False, "sign flip of every code must negate y"
+    # one more in every scale exponent doubles y exactly
+    if not np.array_equal(o.mxfp4_qmv_f64(w, inp.scales + 1, inp.x), 2 * y0):
+        return False, "scale exponent + 1 must double y"
+    # a scale byte of 255 (NaN) poisons its row only
+    s = inp.scales.copy()
+    s[1, 2] = 255
+    yn = o.mxfp4_qmv_f64(w, s, inp.x)
+    if not (np.all(np.isnan(yn[:, 1])) and np.array_equal(yn[:, [0, 2]], y0[:, [0, 2]])):
+        return False, "scale byte 255 must make its row NaN and leave the others"
+    # one-hot x reads one weight: scale * e2m1(code)
+    v = o.e2m1_to_f64(np.arange(16))
+    for k in (0, 31, 32, 77, K - 1):
+        xk = np.zeros((1, K), dtype=np.uint16)
+        xk[0, k] = 0x3F80  # bf16 1.0
+        got = o.mxfp4_qmv_f64(w, inp.scales, xk)[0]
+        want = v[inp.codes[:, k]] * np.ldexp(1.0, inp.scales[:, k // 32].astype(np.int64) - 127)
+        if not np.array_equal(got, want):
+            return False, f"one-hot x at {k}: {got} != {want}"
+    return True, "mxfp4 closed forms: sum(x), zeros, sign flip, scale step, NaN scale, one-hot x"
+
+
 PINS = {
     "bf16_rounding": pin_bf16_rounding,
     "bf16_widen": pin_bf16_widen,
@@ -282,6 +395,11 @@ PINS = {
     "fraction_bruteforce": pin_fraction_bruteforce,
     "closed_forms": pin_closed_forms,
     "f32_form": pin_f32_form,
+    "mx_e2m1_value_set": pin_mx_e2m1_value_set,
+    "mx_e2m1_vs_ml_dtypes": pin_mx_e2m1_vs_ml_dtypes,
+    "mx_e8m0_vs_torch": pin_mx_e8m0_vs_torch,
+    "mx_dequant_vs_numpy": pin_mx_dequant_vs_numpy,
+    "mx_closed_forms": pin_mx_closed_forms,
 }
 
-MUTANTS = tuple(range(1, 8))
+MUTANTS = tuple(range(1, 12))
