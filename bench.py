@@ -2,7 +2,9 @@
 
 One step = one qmv call on the 12B-class decode projection (N=15360, K=3840,
 4-bit affine, group 64, bf16 scale/bias/x, fp32 accumulate, bf16 y), M = 1.
-The same measurement at M = 13 (the streamed kernel) is reported beside it.
+The same measurement at M = 13 (the streamed kernel) is reported beside it,
+and under "mxfp4" the mxfp4 mode (E2M1 codes, one E8M0 scale per 32) on the
+same shape at M = 1 and M = 13.
 
 Device timing: the K steps run as CUDA-graph replays on one stream,
 bracketed by CUDA events; each step reads a different one of R copies of the
@@ -40,6 +42,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "qmv achieved HBM GB/s & % of GB300 roofline at M=1 and M=13 (µs/call)"
 WORKLOAD = "proj_15360x3840_4b_g64"
+MX_WORKLOAD = "proj_15360x3840_mxfp4"
 KERNEL_SOURCES = ["qmv_kernel.cuh", "qmv_plan.h"]
 FALLBACK_HBM_GBS = 6800.0
 
@@ -59,6 +62,11 @@ def kernel_hash() -> str:
 
 def algorithmic_bytes(N, K, M, bits, gs):
     return N * K * bits // 8 + 4 * N * (K // gs) + 2 * M * (K + N)
+
+
+def mx_algorithmic_bytes(N, K, M):
+    """mxfp4: 4-bit codes, one scale byte per 32, bf16 x and y."""
+    return N * K // 2 + N * (K // 32) + 2 * M * (K + N)
 
 
 def max_over_ranks(value: float, world: int, device=None) -> float:
@@ -184,11 +192,16 @@ def run_gpu(args, rank, world, local_rank):
             wq, s, b = sets[i % R]
             g.qmv_run(wq, s, b, x, y, M, N, K, bits, gs, stream=stream)
 
+        return timed(call, args.steps)
+
+    def timed(call, steps):
+        """`warmup` plain calls, then `steps` calls as graph replays between
+        CUDA events on the launch stream; (job milliseconds, clock summary)."""
         with torch.cuda.stream(stream):
             for i in range(args.warmup):
                 call(i)
         torch.cuda.synchronize()
-        n_chunks, rem = divmod(args.steps, chunk)
+        n_chunks, rem = divmod(steps, chunk)
         graphs = []
         with torch.cuda.stream(stream):
             for size in ([chunk] if n_chunks else []) + ([rem] if rem else []):
@@ -247,10 +260,36 @@ def run_gpu(args, rank, world, local_rank):
 
     ms1, clocks1 = measure(1)
     ms13, clocks13 = measure(13)
+
+    # the mxfp4 mode on the same projection shape
+    mxw = synth.MX_WORKLOADS[MX_WORKLOAD]
+    mN, mK = mxw["N"], mxw["K"]
+    minp = synth.make_mxfp4_inputs(mN, mK, 16, seed=0)
+    mw_host = g.qmv_pack(minp.codes, 4)
+    mset_bytes = mw_host.nbytes + minp.scales.nbytes
+    mR = max(2, int(np.ceil(2.0 * l2 / mset_bytes)) + 1)
+    msets = [(tdev(mw_host), torch.from_numpy(np.ascontiguousarray(minp.scales)).to(dev)) for _ in range(mR)]
+    mx_steps = min(args.steps, 50000)
+
+    def measure_mx(M):
+        x = tdev(minp.x[:M])
+        y = torch.empty((M, mN), dtype=torch.int16, device=dev)
+
+        def call(i):
+            wq, sc = msets[i % mR]
+            g.qmv_mxfp4_run(wq, sc, x, y, M, mN, mK, stream=stream)
+
+        return timed(call, mx_steps)
+
+    mx_ms1, _ = measure_mx(1)
+    mx_ms13, mx_clocks13 = measure_mx(13)
+    del msets
     e2e_steps = min(args.steps, 3000)
     e2e_ms, h2d, d2h = measure_e2e(1, e2e_steps)
     return dict(N=N, K=K, bits=bits, gs=gs, R=R, set_bytes=set_bytes, l2=l2, ms1=ms1, ms13=ms13, clocks1=clocks1,
                 clocks13=clocks13, e2e_ms=e2e_ms, e2e_steps=e2e_steps, h2d=h2d, d2h=d2h,
+                mx=dict(N=mN, K=mK, R=mR, set_bytes=mset_bytes, steps=mx_steps, ms1=mx_ms1, ms13=mx_ms13,
+                        clocks13=mx_clocks13),
                 sm_count=torch.cuda.get_device_properties(dev).multi_processor_count)
 
 
@@ -316,6 +355,21 @@ def run_profile(args):
 
     libbuild.build()
     g.load()
+    if args.workload in synth.MX_WORKLOADS:
+        w = synth.MX_WORKLOADS[args.workload]
+        N, K, M = w["N"], w["K"], args.M
+        inp = synth.make_mxfp4_inputs(N, K, M, seed=0)
+        codes = torch.from_numpy(g.qmv_pack(inp.codes, 4).view(np.int32))
+        sets = [(codes.cuda(), torch.from_numpy(inp.scales).cuda()) for _ in range(2)]
+        x = torch.from_numpy(inp.x.view(np.int16)).cuda()
+        y = torch.empty((M, N), dtype=torch.int16, device="cuda")
+        for i in range(args.warmup + args.steps):
+            wd, sd = sets[i % 2]
+            g.qmv_mxfp4_run(wd, sd, x, y, M, N, K)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": args.workload, "M": M, "launches": args.warmup + args.steps,
+                          "bytes_per_launch": mx_algorithmic_bytes(N, K, M)}))
+        return
     w = synth.WORKLOADS[args.workload]
     N, K, bits, gs, M = w["N"], w["K"], w["bits"], w["group_size"], args.M
     inp = synth.make_inputs(N, K, M, bits, gs, seed=0)
@@ -335,6 +389,25 @@ def run_profile(args):
     torch.cuda.synchronize()
     print(json.dumps({"profile": args.workload, "M": M, "launches": args.warmup + args.steps,
                       "bytes_per_launch": algorithmic_bytes(N, K, M, bits, gs)}))
+
+
+def mx_summary(mx, peak, fma_peak_tflops):
+    """The mxfp4 mode's side measurement (same shape, E2M1 codes + E8M0 scales)."""
+    N, K, steps = mx["N"], mx["K"], mx["steps"]
+    out = {"workload": MX_WORKLOAD, "N": N, "K": K, "steps": steps, "kernel": "qmv_mxfp4<V> (V = M)",
+           "l2": f"inputs > L2: {mx['R']} rotating copies of {mx['set_bytes'] / 1e6:.1f} MB"}
+    for M, ms in ((1, mx["ms1"]), (13, mx["ms13"])):
+        us = ms * 1e3 / steps
+        nbytes = mx_algorithmic_bytes(N, K, M)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        d = {"us_per_call": round(us, 3), "achieved_gbs": round(gbs, 2), "hbm_frac": round(gbs / peak, 4),
+             "bytes_per_launch": nbytes}
+        if M > 1:
+            tflops = 2.0 * N * K * M / (us * 1e-6) / 1e12
+            d.update(fp32_tflops=round(tflops, 2), fp32_frac=round(tflops / fma_peak_tflops, 4),
+                     ratio_to_m1=round(ms / mx["ms1"], 3), clocks=mx["clocks13"])
+        out[f"m{M}"] = d
+    return out
 
 
 def main():
@@ -419,6 +492,7 @@ def main():
                     "fp32_lane_peak_tflops": round(fma_peak_tflops, 1),
                     "fp32_frac": round(flops13 / (us13 * 1e-6) / 1e12 / fma_peak_tflops, 4),
                     "kernel": "qmv_streamed<4,64,13>", "bytes_per_launch": b13, "clocks": r["clocks13"]},
+            "mxfp4": mx_summary(r["mx"], peak, fma_peak_tflops),
             "clocks": r["clocks1"],
             "e2e": {"value": round(world * e2e_gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
                     "d2h_bytes_per_step": r["d2h"], "us_per_step": round(r["e2e_ms"] * 1e3, 3),

@@ -1,4 +1,4 @@
-"""Python binding of libqmv.so, the sm_103a affine group-quantized mat-vec.
+"""Python binding of libqmv.so, the sm_103a group-quantized mat-vec (affine and mxfp4).
 
 Argument marshalling only: every step of the computation runs in the CUDA
 library. The names match the C ABI of ``include/qmv.h``. Device buffers may be
@@ -35,7 +35,7 @@ STATUS = {
 }
 
 EXPORTED = ("qmv_packed_words", "qmv_pack", "qmv_unpack", "qmv_pack_sb", "qmv_split_count", "qmv_workspace_size",
-            "qmv_run", "qmv_run_ex", "qmv_run_noalloc", "qmv_workspace_init", "qmv_device_error", "qmv_last_cuda_error",
+            "qmv_run", "qmv_run_ex", "qmv_run_noalloc", "qmv_mxfp4_run", "qmv_workspace_init", "qmv_device_error", "qmv_last_cuda_error",
             "qmv_status_string")
 
 
@@ -81,6 +81,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.qmv_run_ex.argtypes = [P, P, P, P, P, I, I, I, I, I, P, SZ, U, P]
         lib.qmv_run_noalloc.restype = I
         lib.qmv_run_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, P]
+        lib.qmv_mxfp4_run.restype = I
+        lib.qmv_mxfp4_run.argtypes = [P, P, P, P, I, I, I, U, P]
         lib.qmv_workspace_init.restype = I
         lib.qmv_workspace_init.argtypes = [P, SZ, P]
         lib.qmv_device_error.restype = I
@@ -194,6 +196,13 @@ def qmv_run_noalloc(w_q, scales, biases, x, y, M: int, N: int, K: int, bits: int
     code = load().qmv_run_noalloc(_ptr(w_q), _ptr(scales), _ptr(biases), _ptr(x), _ptr(y), M, N, K, bits,
                                   group_size, _stream(stream))
     _check(code, "qmv_run_noalloc")
+
+
+def qmv_mxfp4_run(w_q, scales, x, y, M: int, N: int, K: int, flags: int = 0, stream=None) -> None:
+    """y[M, N] = W x in the mxfp4 mode (E2M1 codes packed by ``qmv_pack(q, 4)``,
+    uint8 E8M0 scales [N, K/32]); see include/qmv.h."""
+    code = load().qmv_mxfp4_run(_ptr(w_q), _ptr(scales), _ptr(x), _ptr(y), M, N, K, int(flags), _stream(stream))
+    _check(code, "qmv_mxfp4_run")
 
 
 def qmv_workspace_init(workspace, nbytes: int, stream=None) -> None:

@@ -21,7 +21,7 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libqmv.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-CU_SOURCES = ["qmv_api.cu", "qmv_noalloc.cu", "qmv_inst_b4g64.cu", "qmv_inst_b4g128.cu", "qmv_inst_b2g64.cu", "qmv_inst_b2g128.cu"]
+CU_SOURCES = ["qmv_api.cu", "qmv_noalloc.cu", "qmv_mx.cu", "qmv_inst_b4g64.cu", "qmv_inst_b4g128.cu", "qmv_inst_b2g64.cu", "qmv_inst_b2g128.cu"]
 CXX_SOURCES = ["qmv_codec.cpp"]
 HEADERS = ["qmv_plan.h", "qmv_kernel.cuh", "qmv_launch.cuh", "qmv_launch_decl.h"]
 

@@ -1,7 +1,8 @@
 // Host side of the C ABI declared in include/qmv.h: argument validation, the
 // launch plans (fixed K-chunks, CTA shape, the one-vector kernel's ring),
 // workspace handling, the scale/bias tensor maps and dispatch to the kernels
-// (M = 1 -> qmv_m1, M = 2..16 -> qmv_streamed with V = M).
+// (M = 1 -> qmv_m1, M = 2..16 -> qmv_streamed with V = M), and the mxfp4
+// entry point (qmv_mxfp4 in qmv_mx.cu for every M).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -541,6 +542,37 @@ extern "C" qmv_status qmv_run_ex(const uint32_t *w_q, const uint16_t *scales, co
 {
     return run_impl(w_q, scales, biases, x, y, M, N, K, bits, group_size, workspace, workspace_bytes, flags,
                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" qmv_status qmv_mxfp4_run(const uint32_t *w_q, const uint8_t *scales, const uint16_t *x, void *y, int M,
+                                    int N, int K, unsigned flags, qmv_stream_t stream)
+{
+    if (!w_q || !scales || !x || !y) return QMV_ERR_NULL;
+    if (N < 1 || N > (1 << 30) || K < 1 || K % 32 != 0 || K > (1 << 24) || (long long)N * (K / 32) >= (1ll << 31))
+        return QMV_ERR_SHAPE;
+    if (M < 1 || M > QMV_MAX_M) return QMV_ERR_M_RANGE;
+    if (flags & ~(QMV_F32_OUT | QMV_FORCE_M1_PER_COLUMN)) return QMV_ERR_FLAGS;
+    const bool f32_out = (flags & QMV_F32_OUT) != 0;
+    if (!aligned(w_q, 16) || !aligned(x, 16) || !aligned(y, f32_out ? 4 : 2)) return QMV_ERR_ALIGN;
+
+    // launches of QMV_TILE_M vectors (one each with QMV_FORCE_M1_PER_COLUMN);
+    // a column's arithmetic does not depend on its launch's width
+    const int tile = (flags & QMV_FORCE_M1_PER_COLUMN) != 0 ? 1 : QMV_TILE_M;
+    const size_t ysize = f32_out ? sizeof(float) : sizeof(uint16_t);
+    qmv::MxParams p;
+    p.w = w_q;
+    p.scales = scales;
+    p.N = N;
+    p.K = K;
+    p.f32_out = f32_out ? 1 : 0;
+    for (int m = 0; m < M; m += tile) {
+        const int V = M - m < tile ? M - m : tile;
+        p.x = x + size_t(m) * K;
+        p.y = static_cast<char *>(y) + size_t(m) * N * ysize;
+        const cudaError_t ce = qmv::launch_mxfp4(V, p, reinterpret_cast<cudaStream_t>(stream));
+        if (ce != cudaSuccess) return cuda_fail("mxfp4 kernel launch", ce);
+    }
+    return QMV_OK;
 }
 
 extern "C" qmv_status qmv_workspace_init(void *workspace, size_t bytes, qmv_stream_t stream)

@@ -26,6 +26,19 @@ struct Launch {
     bool pdl;  // launch with a programmatic dependency on the preceding grid
 };
 
+// Arguments of the mxfp4 kernel (E2M1 codes, one E8M0 byte per 32 along K).
+struct MxParams {
+    const uint32_t *w;       // codes [N][K / 8] words, 8 per word, element 0 in the low nibble
+    const uint8_t *scales;   // E8M0 bytes [N][K / 32]
+    const uint16_t *x;       // bf16 [V][K]
+    void *y;                 // bf16 (or fp32 with f32_out) [V][N]
+    int N, K;                // K a multiple of 32
+    int f32_out;
+};
+
+// One launch for V = 1..16 vectors (qmv_mx.cu).
+cudaError_t launch_mxfp4(int V, const MxParams &p, cudaStream_t stream);
+
 #define QMV_DECLARE_LAUNCH(name)                                                                                  \
     cudaError_t name##_m1(const RingMaps &maps, const RingParams &p, const Launch &l, cudaStream_t stream);      \
     cudaError_t name##_streamed(int V, const Params &p, const Launch &l, cudaStream_t stream);                   \

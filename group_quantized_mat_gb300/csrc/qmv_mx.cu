@@ -1,0 +1,293 @@
+// The mxfp4 mode of qmv: y = W x with E2M1 weights and one E8M0 scale per 32
+// consecutive weights along K.
+//
+// mlxcel issue #1289, section "Scope limits, stated honestly", names the fp
+// modes (mxfp4) as the second phase of the order-preserving streamed qmv and
+// gives no format; the reading taken is the OCP MX v1.0 MXFP4 format: an E2M1
+// element has a sign (bit 3), a 2-bit exponent with bias 1 (bits 2..1) and one
+// mantissa bit (bit 0), exponent field 0 being subnormal; an E8M0 scale byte e
+// is 2^(e - 127), e = 255 being NaN. The codes are packed like the affine
+// 4-bit fields: element k of a row at bits [4 (k % 8), 4 (k % 8) + 4) of word
+// k / 8, so the 32 codes of one scale block are one aligned 16-byte vector.
+//
+// One kernel template serves every launch width V = 1..16, and an output's
+// fp32 operation sequence is the same for every V, so every column of a
+// V-vector launch is bit-identical to the one-vector launch on that column
+// (issue #1289, "The observation this rests on"). For row n and vector m:
+//
+//   1. block b (32 elements): an even chain and an odd chain, each
+//      a = fma(v_i, x_i, a) from +0 in increasing i (both products exact in
+//      fp32: v has two significant bits, x eight), then d_b = a_even + a_odd
+//      and t_b = d_b * 2^(e_b - 127);
+//   2. lane l of the row's warp folds the blocks b = l, l + 32, l + 64, ...
+//      in increasing order: p_l = (((+0 + t_l) + t_{l+32}) + ...);
+//   3. y = p_0 + ... + p_31 by the xor butterfly over offsets 16, 8, 4, 2, 1,
+//      then one rounding to bf16 (nearest even), or the fp32 value itself.
+//
+// The elements come out of the codes by the E2M1 -> f16x2 conversion of
+// sm_100-class parts (two elements per instruction, exact) and one exact
+// f16 -> f32 widening each; the two chains run as one packed fma.rn.f32x2.
+//
+// A CTA holds 8 warps of 4 rows each. K goes by in chunks of 1024 elements,
+// one 32-block per lane; each chunk of x (all V vectors) is staged once per
+// CTA into shared memory as fp32 pairs laid out [vector][pair][lane], so that
+// a warp's read of one pair per lane is 256 contiguous bytes. The next
+// chunk's weight vectors and scale bytes are loaded while the current one is
+// computed. A chunk's weights convert once per pass of up to 4 vectors, and
+// every x pair read from shared memory serves the warp's 4 rows.
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "qmv_launch_decl.h"
+
+namespace qmv {
+namespace {
+
+constexpr int kMxWarps = 8;
+constexpr int kMxRows = 4;                         // rows per warp
+constexpr int kMxRowsPerCta = kMxWarps * kMxRows;  // 32
+constexpr int kMxChunk = 32 * 32;                  // elements per K-chunk: one 32-block per lane
+constexpr int kMxPairs = 16;                       // element pairs per block
+constexpr int kMxPass = 4;                         // vectors per pass over a chunk's weights
+
+// Eight E2M1 codes (one 32-bit word, element 2j in the low nibble of byte j)
+// to four f16x2 words, word j holding elements 2j (low half) and 2j + 1.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4])
+{
+    asm("{\n\t"
+        ".reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t"
+        "}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+}
+
+// f16x2 -> a pair of fp32 in one 64-bit register (low half = low element).
+__device__ __forceinline__ uint64_t f16x2_to_f32x2(uint32_t h)
+{
+    uint64_t d;
+    asm("{\n\t"
+        ".reg .f16 lo, hi;\n\t"
+        ".reg .f32 a, b;\n\t"
+        "mov.b32 {lo, hi}, %1;\n\t"
+        "cvt.f32.f16 a, lo;\n\t"
+        "cvt.f32.f16 b, hi;\n\t"
+        "mov.b64 %0, {a, b};\n\t"
+        "}"
+        : "=l"(d)
+        : "r"(h));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t mx_ffma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// E8M0 byte -> 2^(e - 127) as fp32 (e = 0 is the subnormal 2^-127; 255 is NaN).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t e)
+{
+    const uint32_t bits = e == 0u ? 0x00400000u : (e == 255u ? 0x7fc00000u : e << 23);
+    return __uint_as_float(bits);
+}
+
+// Stages x[v][k0 .. k0 + kn) for v < V into xs[v][pair][lane] as fp32 pairs
+// (element 32 l + 2 i in the low half of xs[v][i][l]). kn is a multiple of 32.
+template <int V>
+__device__ __forceinline__ void mx_stage_chunk(uint64_t *xs, const uint16_t *x, int K, int k0, int kn)
+{
+    for (int item = threadIdx.x; item < V * (kMxChunk / 8); item += kMxWarps * 32) {
+        const int v = item / (kMxChunk / 8);
+        const int e0 = (item % (kMxChunk / 8)) * 8;
+        if (e0 >= kn) continue;
+        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(x + size_t(v) * K + k0 + e0));
+        uint64_t *dst = xs + (size_t(v) * kMxPairs + ((e0 & 31) >> 1)) * 32 + (e0 >> 5);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            dst[q * 32] = (uint64_t(w[q] & 0xffff0000u) << 32) | uint64_t(w[q] << 16);
+    }
+}
+
+template <int V>
+__global__ void __launch_bounds__(kMxWarps * 32) qmv_mxfp4(MxParams p)
+{
+    extern __shared__ __align__(16) uint64_t mx_xs[];  // [V][kMxPairs][32] fp32 pairs
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int row0 = blockIdx.x * kMxRowsPerCta + warp * kMxRows;
+    const int B = p.K >> 5;  // scale blocks per row
+    const int nchunks = (B + 31) >> 5;
+
+    const uint4 *wrow[kMxRows];
+    const uint8_t *srow[kMxRows];
+    bool live[kMxRows];
+#pragma unroll
+    for (int r = 0; r < kMxRows; ++r) {
+        live[r] = row0 + r < p.N;
+        const size_t n = size_t(live[r] ? row0 + r : p.N - 1);
+        wrow[r] = reinterpret_cast<const uint4 *>(p.w) + n * B;  // one 16-byte vector per block
+        srow[r] = p.scales + n * B;
+    }
+
+    float part[V][kMxRows];
+#pragma unroll
+    for (int v = 0; v < V; ++v)
+#pragma unroll
+        for (int r = 0; r < kMxRows; ++r) part[v][r] = 0.0f;
+
+    uint4 wc[kMxRows];
+    uint32_t sc[kMxRows];
+#pragma unroll
+    for (int r = 0; r < kMxRows; ++r) {
+        const bool ok = live[r] && lane < B;
+        wc[r] = ok ? __ldg(wrow[r] + lane) : make_uint4(0u, 0u, 0u, 0u);
+        sc[r] = ok ? __ldg(srow[r] + lane) : 0u;
+    }
+
+    for (int c = 0; c < nchunks; ++c) {
+        const int k0 = c * kMxChunk;
+        const int kn = p.K - k0 < kMxChunk ? p.K - k0 : kMxChunk;
+        __syncthreads();  // every warp is done reading the previous chunk of x
+        mx_stage_chunk<V>(mx_xs, p.x, p.K, k0, kn);
+        __syncthreads();
+
+        // next chunk's weights and scales, in flight while this one is computed
+        uint4 wn[kMxRows];
+        uint32_t sn[kMxRows];
+        const int bn = (c + 1) * 32 + lane;
+#pragma unroll
+        for (int r = 0; r < kMxRows; ++r) {
+            const bool ok = live[r] && bn < B;
+            wn[r] = ok ? __ldg(wrow[r] + bn) : make_uint4(0u, 0u, 0u, 0u);
+            sn[r] = ok ? __ldg(srow[r] + bn) : 0u;
+        }
+
+        if (c * 32 + lane < B) {
+            float scale[kMxRows];
+#pragma unroll
+            for (int r = 0; r < kMxRows; ++r) scale[r] = e8m0_to_f32(sc[r]);
+#pragma unroll
+            for (int v0 = 0; v0 < V; v0 += kMxPass) {
+                uint64_t acc[kMxPass][kMxRows];
+#pragma unroll
+                for (int v = 0; v < kMxPass; ++v)
+#pragma unroll
+                    for (int r = 0; r < kMxRows; ++r) acc[v][r] = 0ull;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t h[kMxRows][4];
+#pragma unroll
+                    for (int r = 0; r < kMxRows; ++r) {
+                        const uint32_t word = j == 0 ? wc[r].x : j == 1 ? wc[r].y : j == 2 ? wc[r].z : wc[r].w;
+                        e2m1x8_to_f16x2(word, h[r]);
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int i = 4 * j + k;
+                        uint64_t wv[kMxRows];
+#pragma unroll
+                        for (int r = 0; r < kMxRows; ++r) wv[r] = f16x2_to_f32x2(h[r][k]);
+#pragma unroll
+                        for (int v = 0; v < kMxPass; ++v) {
+                            if (v0 + v >= V) continue;
+                            const uint64_t xv = mx_xs[((v0 + v) * kMxPairs + i) * 32 + lane];
+#pragma unroll
+                            for (int r = 0; r < kMxRows; ++r) acc[v][r] = mx_ffma2(wv[r], xv, acc[v][r]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int v = 0; v < kMxPass; ++v) {
+                    if (v0 + v >= V) continue;
+#pragma unroll
+                    for (int r = 0; r < kMxRows; ++r) {
+                        const float ae = __uint_as_float(uint32_t(acc[v][r]));
+                        const float ao = __uint_as_float(uint32_t(acc[v][r] >> 32));
+                        const float t = __fmul_rn(__fadd_rn(ae, ao), scale[r]);
+                        part[v0 + v][r] = __fadd_rn(part[v0 + v][r], t);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kMxRows; ++r) {
+            wc[r] = wn[r];
+            sc[r] = sn[r];
+        }
+    }
+
+    // butterfly over the lanes: every lane ends with the same sum
+#pragma unroll
+    for (int v = 0; v < V; ++v)
+#pragma unroll
+        for (int r = 0; r < kMxRows; ++r) {
+            float s = part[v][r];
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, off));
+            part[v][r] = s;
+        }
+#pragma unroll
+    for (int r = 0; r < kMxRows; ++r) {
+        if (lane != r || !live[r]) continue;
+        const size_t n = size_t(row0 + r);
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            if (p.f32_out)
+                static_cast<float *>(p.y)[size_t(v) * p.N + n] = part[v][r];
+            else
+                static_cast<__nv_bfloat16 *>(p.y)[size_t(v) * p.N + n] = __float2bfloat16_rn(part[v][r]);
+        }
+    }
+}
+
+template <int V>
+cudaError_t launch_mx_v(const MxParams &p, cudaStream_t stream)
+{
+    // The opt-in dynamic shared-memory limit is a per-device kernel attribute;
+    // raise it (never lower it) under a lock the first time a device needs it.
+    static std::atomic<int> configured[64] = {};
+    const int smem = V * kMxPairs * 32 * int(sizeof(uint64_t));
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64) return cudaErrorInvalidDevice;
+    if (configured[dev].load() < smem) {
+        static std::mutex m;
+        std::lock_guard<std::mutex> lock(m);
+        if (configured[dev].load() < smem) {
+            e = cudaFuncSetAttribute(qmv_mxfp4<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+            configured[dev].store(smem);
+        }
+    }
+    const unsigned grid = unsigned((p.N + kMxRowsPerCta - 1) / kMxRowsPerCta);
+    qmv_mxfp4<V><<<grid, kMxWarps * 32, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_mxfp4(int V, const MxParams &p, cudaStream_t stream)
+{
+    switch (V) {
+#define QMV_MX_CASE(v) \
+    case v: return launch_mx_v<v>(p, stream);
+        QMV_MX_CASE(1) QMV_MX_CASE(2) QMV_MX_CASE(3) QMV_MX_CASE(4) QMV_MX_CASE(5) QMV_MX_CASE(6)
+        QMV_MX_CASE(7) QMV_MX_CASE(8) QMV_MX_CASE(9) QMV_MX_CASE(10) QMV_MX_CASE(11) QMV_MX_CASE(12)
+        QMV_MX_CASE(13) QMV_MX_CASE(14) QMV_MX_CASE(15) QMV_MX_CASE(16)
+#undef QMV_MX_CASE
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace qmv

@@ -1,5 +1,6 @@
 /*
- * qmv.h -- C ABI of the GB300 (sm_103a) affine group-quantized mat-vec library.
+ * qmv.h -- C ABI of the GB300 (sm_103a) group-quantized mat-vec library: the
+ * affine mode below, and the mxfp4 mode (qmv_mxfp4_run).
  *
  *   y[m, n] = sum_i ( s[n, i/gs] * q[n, i] + b[n, i/gs] ) * x[m, i]
  *
@@ -213,6 +214,56 @@ QMV_API qmv_status qmv_run_ex(const uint32_t *w_q, const uint16_t *scales, const
 QMV_API qmv_status qmv_run_noalloc(const uint32_t *w_q, const uint16_t *scales, const uint16_t *biases,
                                    const uint16_t *x, uint16_t *y, int M, int N, int K, int bits,
                                    int group_size, qmv_stream_t stream);
+
+/* ------------------------------------------------------------------ mxfp4 */
+
+/* y = W . x in the mxfp4 mode, asynchronously on `stream`:
+ *
+ *   y[m, n] = sum_i 2^(e[n, i/32] - 127) * e2m1(q[n, i]) * x[m, i]
+ *
+ * The pages name an order-preserving streamed qmv for the fp quantization
+ * modes ("mxfp4") as the second phase of the work (issue #1289, "Scope limits,
+ * stated honestly") without giving the format; this is the OCP MX v1.0 MXFP4
+ * format:
+ *  - element: E2M1 code: sign (bit 3), exponent (bits 2..1, bias 1) and
+ *    mantissa (bit 0). Exponent 0 is subnormal, so the values are
+ *    +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}.
+ *  - scale: one E8M0 byte e per 32 consecutive elements along K, 2^(e - 127);
+ *    e = 255 is NaN.
+ *
+ *  w_q     device, uint32 [N, K/8], 16-byte aligned: the codes packed as 4-bit
+ *          fields exactly as qmv_pack(q, w_q, N, K, 4) packs them (element 0
+ *          in the low nibble), so each 32-block is one 16-byte vector.
+ *  scales  device, uint8 [N, K/32], row-major (no alignment needed).
+ *  x       device, bf16 [M, K], row-major, 16-byte aligned.
+ *  y       device, bf16 [M, N] (fp32 with QMV_F32_OUT), row-major; no overlap
+ *          with any input.
+ *  M       1 .. QMV_MAX_M (launches of QMV_TILE_M vectors). N >= 1,
+ *          K >= 32 and a multiple of 32.
+ *  flags   QMV_F32_OUT and QMV_FORCE_M1_PER_COLUMN (as for qmv_run_ex).
+ *
+ * Arithmetic is fp32 in a fixed order that depends only on K and the
+ * element's row, never on M:
+ *  1. Each block of 32 forms two fma chains, over its even and its odd
+ *     elements. The products are exact.
+ *  2. The chain sums are added, then multiplied by the block's scale.
+ *  3. Blocks b = l, l+32, l+64, ... are folded in order into partial l, for
+ *     l = 0..31.
+ *  4. The 32 partials are summed by a fixed xor tree.
+ *  5. The result is rounded once to bf16.
+ * So column j of an M-vector call is bit-identical to an M = 1 call on x[j].
+ * No workspace and no device allocation: the call may be captured in a CUDA
+ * graph.
+ *
+ * Errors:
+ *  - QMV_ERR_NULL.
+ *  - QMV_ERR_SHAPE: N < 1, K < 1, K % 32 != 0, N > 2^30, K > 2^24, or
+ *    N * K/32 >= 2^31.
+ *  - QMV_ERR_M_RANGE, QMV_ERR_ALIGN, QMV_ERR_FLAGS.
+ *  - QMV_ERR_CUDA when a launch fails.
+ * The host checks run before anything is launched. */
+QMV_API qmv_status qmv_mxfp4_run(const uint32_t *w_q, const uint8_t *scales, const uint16_t *x, void *y,
+                                 int M, int N, int K, unsigned flags, qmv_stream_t stream);
 
 /* Zero-fills `bytes` of a caller workspace on `stream` (cudaMemsetAsync). Calls
  * do not need it (a workspace holds no state between calls); kept as a

@@ -186,3 +186,21 @@ def test_status_strings(lib):
         s = g.qmv_status_string(code)
         assert s.startswith(g.STATUS[code])
     assert "unknown" in g.qmv_status_string(99)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(w_q=0), 1), (dict(scales=0), 1), (dict(x=0), 1), (dict(y=0), 1),
+    (dict(K=48), 4), (dict(K=0), 4), (dict(N=0), 4), (dict(K=1 << 25), 4), (dict(N=(1 << 30) + 1), 4),
+    (dict(N=1 << 26, K=1 << 10), 4),  # N * K/32 = 2^31 scale bytes
+    (dict(M=0), 5), (dict(M=257), 5),
+    (dict(w_q=FAKE + 8), 6), (dict(x=FAKE + 2), 6), (dict(y=FAKE + 1), 6),
+    (dict(flags=0x4), 10), (dict(flags=0x8), 10), (dict(flags=0x100), 10),
+])
+def test_mxfp4_run_validation_before_gpu(lib, kw, code):
+    args = dict(w_q=FAKE, scales=FAKE + 3, x=FAKE, y=FAKE, M=1, N=64, K=1024, flags=0)
+    args.update(kw)
+    r = lib.qmv_mxfp4_run(args["w_q"] or None, args["scales"] or None, args["x"] or None, args["y"] or None,
+                          args["M"], args["N"], args["K"], args["flags"], None)
+    assert r == code, g.qmv_status_string(r)
+    # an fp32 y needs 4-byte alignment
+    assert lib.qmv_mxfp4_run(FAKE, FAKE, FAKE, FAKE + 2, 1, 64, 1024, g.F32_OUT, None) == 6
