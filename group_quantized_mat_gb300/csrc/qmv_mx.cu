@@ -31,9 +31,10 @@
 // A CTA holds 8 warps of 4 rows each. K goes by in chunks of 1024 elements,
 // one 32-block per lane; each chunk of x (all V vectors) is staged once per
 // CTA into shared memory as fp32 pairs laid out [vector][pair][lane], so that
-// a warp's read of one pair per lane is 256 contiguous bytes. The next
-// chunk's weight vectors and scale bytes are loaded while the current one is
-// computed. A chunk's weights convert once per pass of up to 4 vectors, and
+// a warp's read of one pair per lane is 256 contiguous bytes. With several
+// vectors the next chunk's weight vectors and scale bytes are loaded while the
+// current one is computed. A chunk's weights convert once per pass of up to 4
+// vectors, and
 // every x pair read from shared memory serves the warp's 4 rows.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -103,15 +104,19 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t e)
 
 // Stages x[v][k0 .. k0 + kn) for v < V into xs[v][pair][lane] as fp32 pairs
 // (element 32 l + 2 i in the low half of xs[v][i][l]). kn is a multiple of 32.
+// Thread item t of a vector takes the 8 elements (t / 32) * 8 .. + 7 of block
+// t % 32, so the 32 threads of a warp write 32 consecutive lanes of one pair
+// row: every shared-memory store is conflict-free.
 template <int V>
 __device__ __forceinline__ void mx_stage_chunk(uint64_t *xs, const uint16_t *x, int K, int k0, int kn)
 {
     for (int item = threadIdx.x; item < V * (kMxChunk / 8); item += kMxWarps * 32) {
         const int v = item / (kMxChunk / 8);
-        const int e0 = (item % (kMxChunk / 8)) * 8;
+        const int blk = item % 32, quad = (item % (kMxChunk / 8)) / 32;
+        const int e0 = blk * 32 + quad * 8;
         if (e0 >= kn) continue;
         const uint4 u = __ldg(reinterpret_cast<const uint4 *>(x + size_t(v) * K + k0 + e0));
-        uint64_t *dst = xs + (size_t(v) * kMxPairs + ((e0 & 31) >> 1)) * 32 + (e0 >> 5);
+        uint64_t *dst = xs + (size_t(v) * kMxPairs + quad * 4) * 32 + blk;
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q)
@@ -119,8 +124,14 @@ __device__ __forceinline__ void mx_stage_chunk(uint64_t *xs, const uint16_t *x, 
     }
 }
 
+// CTAs per SM the register budget must allow: four for one vector (at most
+// 64 registers), so that a 15360-row matrix (480 CTAs) runs as one wave on
+// 152 SMs; two for 2..4 vectors.
 template <int V>
-__global__ void __launch_bounds__(kMxWarps * 32) qmv_mxfp4(MxParams p)
+constexpr int mx_min_blocks() { return V == 1 ? 4 : V <= 4 ? 2 : 1; }
+
+template <int V>
+__global__ void __launch_bounds__(kMxWarps * 32, mx_min_blocks<V>()) qmv_mxfp4(MxParams p)
 {
     extern __shared__ __align__(16) uint64_t mx_xs[];  // [V][kMxPairs][32] fp32 pairs
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -128,16 +139,10 @@ __global__ void __launch_bounds__(kMxWarps * 32) qmv_mxfp4(MxParams p)
     const int B = p.K >> 5;  // scale blocks per row
     const int nchunks = (B + 31) >> 5;
 
-    const uint4 *wrow[kMxRows];
-    const uint8_t *srow[kMxRows];
-    bool live[kMxRows];
-#pragma unroll
-    for (int r = 0; r < kMxRows; ++r) {
-        live[r] = row0 + r < p.N;
-        const size_t n = size_t(live[r] ? row0 + r : p.N - 1);
-        wrow[r] = reinterpret_cast<const uint4 *>(p.w) + n * B;  // one 16-byte vector per block
-        srow[r] = p.scales + n * B;
-    }
+    // rows row0 .. row0 + nlive - 1 exist; one 16-byte vector of codes per block
+    const int nlive = p.N - row0;
+    const uint4 *wbase = reinterpret_cast<const uint4 *>(p.w) + size_t(row0) * B;
+    const uint8_t *sbase = p.scales + size_t(row0) * B;
 
     float part[V][kMxRows];
 #pragma unroll
@@ -145,32 +150,35 @@ __global__ void __launch_bounds__(kMxWarps * 32) qmv_mxfp4(MxParams p)
 #pragma unroll
         for (int r = 0; r < kMxRows; ++r) part[v][r] = 0.0f;
 
+    // The codes and scale bytes of block b for the warp's rows.
+    auto load_block = [&](int b, uint4 (&w)[kMxRows], uint32_t (&sv)[kMxRows]) {
+#pragma unroll
+        for (int r = 0; r < kMxRows; ++r) {
+            const bool ok = r < nlive && b < B;
+            w[r] = ok ? __ldg(wbase + size_t(r) * B + b) : make_uint4(0u, 0u, 0u, 0u);
+            sv[r] = ok ? __ldg(sbase + size_t(r) * B + b) : 0u;
+        }
+    };
+    // Several vectors: the next chunk's loads are issued a chunk ahead. One
+    // vector: a chunk's loads are issued before its x is staged; the four CTAs
+    // an SM then holds keep enough of them in flight, and the 64-register
+    // budget has no room for a second set.
+    constexpr bool kAhead = V > 1;
     uint4 wc[kMxRows];
     uint32_t sc[kMxRows];
-#pragma unroll
-    for (int r = 0; r < kMxRows; ++r) {
-        const bool ok = live[r] && lane < B;
-        wc[r] = ok ? __ldg(wrow[r] + lane) : make_uint4(0u, 0u, 0u, 0u);
-        sc[r] = ok ? __ldg(srow[r] + lane) : 0u;
-    }
+    if (kAhead) load_block(lane, wc, sc);
 
     for (int c = 0; c < nchunks; ++c) {
         const int k0 = c * kMxChunk;
         const int kn = p.K - k0 < kMxChunk ? p.K - k0 : kMxChunk;
+        if (!kAhead) load_block(c * 32 + lane, wc, sc);
         __syncthreads();  // every warp is done reading the previous chunk of x
         mx_stage_chunk<V>(mx_xs, p.x, p.K, k0, kn);
         __syncthreads();
 
-        // next chunk's weights and scales, in flight while this one is computed
         uint4 wn[kMxRows];
         uint32_t sn[kMxRows];
-        const int bn = (c + 1) * 32 + lane;
-#pragma unroll
-        for (int r = 0; r < kMxRows; ++r) {
-            const bool ok = live[r] && bn < B;
-            wn[r] = ok ? __ldg(wrow[r] + bn) : make_uint4(0u, 0u, 0u, 0u);
-            sn[r] = ok ? __ldg(srow[r] + bn) : 0u;
-        }
+        if (kAhead) load_block((c + 1) * 32 + lane, wn, sn);
 
         if (c * 32 + lane < B) {
             float scale[kMxRows];
@@ -219,10 +227,12 @@ __global__ void __launch_bounds__(kMxWarps * 32) qmv_mxfp4(MxParams p)
                 }
             }
         }
+        if (kAhead) {
 #pragma unroll
-        for (int r = 0; r < kMxRows; ++r) {
-            wc[r] = wn[r];
-            sc[r] = sn[r];
+            for (int r = 0; r < kMxRows; ++r) {
+                wc[r] = wn[r];
+                sc[r] = sn[r];
+            }
         }
     }
 
@@ -238,7 +248,7 @@ __global__ void __launch_bounds__(kMxWarps * 32) qmv_mxfp4(MxParams p)
         }
 #pragma unroll
     for (int r = 0; r < kMxRows; ++r) {
-        if (lane != r || !live[r]) continue;
+        if (lane != r || r >= nlive) continue;
         const size_t n = size_t(row0 + r);
 #pragma unroll
         for (int v = 0; v < V; ++v) {
