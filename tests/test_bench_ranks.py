@@ -61,3 +61,24 @@ def test_reference_arm_under_torchrun_prints_once():
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_mxfp4_bytes_and_summary():
+    """The mxfp4 side measurement: algorithmic bytes (4-bit codes, one scale byte
+    per 32, bf16 x and y) and the fields and fractions of its JSON object."""
+    sys.path.insert(0, ROOT)
+    import bench
+    N, K = 15360, 3840
+    assert bench.mx_algorithmic_bytes(N, K, 1) == N * K // 2 + N * K // 32 + 2 * (K + N) == 31372800
+    assert bench.mx_algorithmic_bytes(N, K, 13) == 31372800 + 12 * 2 * (K + N)
+    mx = dict(N=N, K=K, R=10, set_bytes=31334400, steps=1000, ms1=12.0, ms13=84.0,
+              clocks13={"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 9})
+    out = bench.mx_summary(mx, 6773.5, 80.5)
+    assert out["workload"] == bench.MX_WORKLOAD and out["N"] == N and out["K"] == K
+    m1, m13 = out["m1"], out["m13"]
+    assert m1["us_per_call"] == 12.0 and m13["us_per_call"] == 84.0
+    assert abs(m1["achieved_gbs"] - 31372800 / 12e-6 / 1e9) < 0.01
+    assert abs(m1["hbm_frac"] - m1["achieved_gbs"] / 6773.5) < 1e-4
+    assert abs(m13["fp32_tflops"] - 2.0 * N * K * 13 / 84e-6 / 1e12) < 0.01
+    assert abs(m13["fp32_frac"] - m13["fp32_tflops"] / 80.5) < 1e-3
+    assert m13["ratio_to_m1"] == 7.0 and m13["clocks"]["reasons"] == []
