@@ -294,8 +294,9 @@ def run_gpu(args, rank, world, local_rank):
 
 
 # --------------------------------------------------------------------------- CPU oracle
-def oracle_timing(N, K, M, bits, gs, seconds=10.0, rows=None, repeats=None):
-    """fp32 factored oracle on all host cores; returns (seconds per run, threads, rows, runs)."""
+def oracle_timing(N, K, M, bits, gs, seconds=10.0, rows=None, repeats=None, threads=None):
+    """fp32 factored oracle on `threads` host cores (all of them by default);
+    returns (seconds per run, threads used, rows, runs)."""
     import synth
     from oracle import Oracle
     o = Oracle(0)
@@ -303,7 +304,7 @@ def oracle_timing(N, K, M, bits, gs, seconds=10.0, rows=None, repeats=None):
     rows = N if rows is None else rows
     wq = o.pack(inp.q[:rows], bits)
     s, b = inp.scales[:rows], inp.biases[:rows]
-    threads = len(os.sched_getaffinity(0))
+    threads = len(os.sched_getaffinity(0)) if threads is None else int(threads)
     o.qmv_f32_factored(wq, s, b, inp.x, bits, gs, nthreads=threads)  # warm
     runs, t0 = 0, time.perf_counter()
     used = threads
@@ -456,6 +457,11 @@ def main():
         peak, peak_kind = measured_peaks()
         cpu_t, cpu_threads, cpu_rows, cpu_runs = oracle_timing(N, K, 1, bits, gs, seconds=args.cpu_seconds)
         cpu_gbs = b1 / cpu_t / 1e9
+        # the same oracle on one core, over the first 1/16 of the rows
+        one_rows = max(1, N // 16)
+        one_t, _, _, one_runs = oracle_timing(N, K, 1, bits, gs, seconds=min(3.0, args.cpu_seconds), rows=one_rows,
+                                              threads=1)
+        one_gbs = algorithmic_bytes(one_rows, K, 1, bits, gs) / one_t / 1e9
         e2e_gbs = b1 / (r["e2e_ms"] * 1e-3) / 1e9
         kh = kernel_hash()
         traffic = NCU_TRAFFIC.get(kh)
@@ -499,7 +505,9 @@ def main():
                     "steps": r["e2e_steps"], "api": "group_quantized_mat_gb300.qmv_run (C ABI qmv_run)"},
             "gpu_launches": args.steps,
             "cpu_baseline": {"value": round(cpu_gbs, 4), "unit": "GB/s", "cores": cpu_threads, "kind": "oracle",
-                             "sample": f"full {N}x{K} M=1 problem (fp32 factored oracle), {cpu_runs} runs"},
+                             "sample": f"full {N}x{K} M=1 problem (fp32 factored oracle), {cpu_runs} runs",
+                             "single_core": {"value": round(one_gbs, 4), "unit": "GB/s", "cores": 1,
+                                             "sample": f"rows 0..{one_rows - 1} of the same problem, {one_runs} runs"}},
             "kernel_hash": kh,
         }
         print(json.dumps(line), flush=True)
