@@ -204,3 +204,38 @@ def test_mxfp4_run_validation_before_gpu(lib, kw, code):
     assert r == code, g.qmv_status_string(r)
     # an fp32 y needs 4-byte alignment
     assert lib.qmv_mxfp4_run(FAKE, FAKE, FAKE, FAKE + 2, 1, 64, 1024, g.F32_OUT, None) == 6
+
+
+def test_header_compiles_as_c_and_links(tmp_path, lib):
+    """include/qmv.h is a plain C header: a C99 program that includes it,
+    calls the host-only entry points and links against libqmv.so runs
+    without a GPU."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "use_qmv.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include "qmv.h"
+int main(void) {
+    uint8_t q[64];
+    uint32_t w[8];
+    for (int i = 0; i < 64; ++i) q[i] = (uint8_t)(i % 16);
+    if (qmv_packed_words(1, 64, 4) != 8) return 1;
+    if (qmv_pack(q, w, 1, 64, 4) != QMV_OK) return 2;
+    if (w[0] != 0x76543210u) return 3;
+    if (qmv_mxfp4_run(NULL, NULL, NULL, NULL, 1, 1, 32, 0u, NULL) != QMV_ERR_NULL) return 4;
+    printf("%s\n", qmv_status_string(QMV_ERR_SHAPE));
+    return 0;
+}
+''')
+    inc = os.path.join(ROOT, "include")
+    libdir = os.path.dirname(g.LIB_PATH)
+    exe = tmp_path / "use_qmv"
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", inc, str(src), "-L", libdir, "-lqmv",
+                        f"-Wl,-rpath,{libdir}", "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stderr)
+    assert r.stdout.strip() != ""
