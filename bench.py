@@ -392,11 +392,35 @@ def run_profile(args):
                       "bytes_per_launch": algorithmic_bytes(N, K, M, bits, gs)}))
 
 
-def mx_summary(mx, peak, fma_peak_tflops):
-    """The mxfp4 mode's side measurement (same shape, E2M1 codes + E8M0 scales)."""
+def mx_oracle_timing(K, rows=256, seconds=2.0):
+    """The mxfp4 oracle (fp64 dequantize-then-dot, one thread) on `rows` rows of
+    the workload's shape and distribution, M = 1: (seconds per run, runs)."""
+    import synth
+    from oracle import Oracle
+    o = Oracle(0)
+    inp = synth.make_mxfp4_inputs(rows, K, 1, seed=0)
+    wq = o.pack(inp.codes, 4)
+    o.mxfp4_qmv_f64(wq, inp.scales, inp.x)  # warm
+    runs, t0 = 0, time.perf_counter()
+    while True:
+        o.mxfp4_qmv_f64(wq, inp.scales, inp.x)
+        runs += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return el / runs, runs
+
+
+def mx_summary(mx, peak, fma_peak_tflops, cpu=None):
+    """The mxfp4 mode's side measurement (same shape, E2M1 codes + E8M0 scales).
+    `cpu` = (rows, seconds per run, runs) of the oracle timed beside it, or None."""
     N, K, steps = mx["N"], mx["K"], mx["steps"]
     out = {"workload": MX_WORKLOAD, "N": N, "K": K, "steps": steps, "kernel": "qmv_mxfp4<V> (V = M)",
            "l2": f"inputs > L2: {mx['R']} rotating copies of {mx['set_bytes'] / 1e6:.1f} MB"}
+    if cpu is not None:
+        rows, t, runs = cpu
+        out["cpu_oracle"] = {"value": round(mx_algorithmic_bytes(rows, K, 1) / t / 1e9, 5), "unit": "GB/s",
+                             "cores": 1, "kind": "oracle",
+                             "sample": f"{rows} rows x {K}, M=1, fp64 dequantize-then-dot, {runs} runs"}
     for M, ms in ((1, mx["ms1"]), (13, mx["ms13"])):
         us = ms * 1e3 / steps
         nbytes = mx_algorithmic_bytes(N, K, M)
@@ -498,7 +522,7 @@ def main():
                     "fp32_lane_peak_tflops": round(fma_peak_tflops, 1),
                     "fp32_frac": round(flops13 / (us13 * 1e-6) / 1e12 / fma_peak_tflops, 4),
                     "kernel": "qmv_streamed<4,64,13>", "bytes_per_launch": b13, "clocks": r["clocks13"]},
-            "mxfp4": mx_summary(r["mx"], peak, fma_peak_tflops),
+            "mxfp4": mx_summary(r["mx"], peak, fma_peak_tflops, cpu=(256, *mx_oracle_timing(r["mx"]["K"]))),
             "clocks": r["clocks1"],
             "e2e": {"value": round(world * e2e_gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
                     "d2h_bytes_per_step": r["d2h"], "us_per_step": round(r["e2e_ms"] * 1e3, 3),

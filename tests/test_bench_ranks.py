@@ -82,3 +82,9 @@ def test_mxfp4_bytes_and_summary():
     assert abs(m13["fp32_tflops"] - 2.0 * N * K * 13 / 84e-6 / 1e12) < 0.01
     assert abs(m13["fp32_frac"] - m13["fp32_tflops"] / 80.5) < 1e-3
     assert m13["ratio_to_m1"] == 7.0 and m13["clocks"]["reasons"] == []
+    assert "cpu_oracle" not in out
+    t, runs = bench.mx_oracle_timing(K, rows=8, seconds=0.05)
+    assert t > 0 and runs >= 1
+    cpu = bench.mx_summary(mx, 6773.5, 80.5, cpu=(8, t, runs))["cpu_oracle"]
+    assert cpu["kind"] == "oracle" and cpu["cores"] == 1
+    assert abs(cpu["value"] - bench.mx_algorithmic_bytes(8, K, 1) / t / 1e9) < 1e-4
