@@ -343,6 +343,24 @@ def pin_mx_dequant_vs_numpy(o):
     return True, "mxfp4 fp64 dequantize-then-dot agrees with numpy over library-decoded weights"
 
 
+def pin_mx_fraction_bruteforce(o):
+    """Exact rational sums over library-decoded weights on tiny shapes: the fp64
+    oracle must sit within 1e-13 * sum|w x| of them."""
+    for K in (32, 64, 160):
+        inp = synth.make_mxfp4_inputs(3, K, 2, seed=50 + K)
+        W = _mx_decode_numpy(inp.codes, inp.scales)
+        xf = _f64(inp.x)
+        w = o.pack(inp.codes, 4)
+        y = o.mxfp4_qmv_f64(w, inp.scales, inp.x)
+        T = o.mxfp4_abs_terms(w, inp.scales, inp.x)
+        for m in range(2):
+            for n in range(3):
+                ex = sum((Fraction(float(W[n, i])) * Fraction(float(xf[m, i])) for i in range(K)), Fraction(0))
+                if abs(Fraction(float(y[m, n])) - ex) > Fraction(1e-13) * Fraction(float(T[m, n])):
+                    return False, f"mxfp4 brute force K={K} ({m},{n})"
+    return True, "mxfp4 fp64 oracle matches exact rational arithmetic"
+
+
 def pin_mx_closed_forms(o):
     import math
     N, K = 3, 128
@@ -399,6 +417,7 @@ PINS = {
     "mx_e2m1_vs_ml_dtypes": pin_mx_e2m1_vs_ml_dtypes,
     "mx_e8m0_vs_torch": pin_mx_e8m0_vs_torch,
     "mx_dequant_vs_numpy": pin_mx_dequant_vs_numpy,
+    "mx_fraction_bruteforce": pin_mx_fraction_bruteforce,
     "mx_closed_forms": pin_mx_closed_forms,
 }
 

@@ -176,6 +176,21 @@ def test_mxfp4_full_size_sampled_rows(o, N, K, M):
     check(y[:, rows], y_ref, terms, f"mxfp4 {N}x{K} M={M} sampled")
 
 
+@pytest.mark.parametrize("M", [1, 3])
+def test_mxfp4_long_rows(o, M):
+    """K = 2^22: 4096 chunks per row; every column still equals its one-vector
+    call bit for bit."""
+    N, K = 5, 1 << 22
+    inp = synth.make_mxfp4_inputs(N, K, M, seed=90 + M)
+    d = MxDevice(inp)
+    y = d.run(flags=g.F32_OUT)
+    if M > 1:
+        singles = np.stack([d.run(x=d.x[m:m + 1].contiguous(), M=1, flags=g.F32_OUT)[0] for m in range(M)])
+        assert np.array_equal(y.view(np.uint32), singles.view(np.uint32))
+    y_ref, terms = oracle_rows(o, inp)
+    check(d.run(), y_ref, terms, f"mxfp4 K=2^22 M={M}")
+
+
 def test_mxfp4_graph_capture_replays_identically():
     inp = synth.make_mxfp4_inputs(512, 3840, 13, seed=30)
     d = MxDevice(inp)
