@@ -156,6 +156,14 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- GPU arm
+EXTRA_STEPS = 2000        # calls per side measurement (at most --steps)
+WARM_CALLS = 2000         # untimed calls queued right before every timed region
+SWEEP_MS = (1, 2, 4, 5, 10, 13, 16)
+STACK = ("l27b_5120x5120_4b_g64", "l27b_1024x5120_4b_g64", "l27b_17408x5120_4b_g64", "l27b_5120x17408_4b_g64")
+TWO_BIT = ("proj_15360x3840_2b_g64", "proj_15360x3840_2b_g128")
+CHUNK = 500               # calls per captured graph
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
 
@@ -167,74 +175,121 @@ def run_gpu(args, rank, world, local_rank):
     g.load()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = synth.WORKLOADS[WORKLOAD]
-    N, K, bits, gs = w["N"], w["K"], w["bits"], w["group_size"]
-    inp = synth.make_inputs(N, K, 16, bits, gs, seed=0)
-    w_host = g.qmv_pack(inp.q, bits)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    stream = torch.cuda.Stream(device=dev)
 
     def tdev(a):
         a = a.view(np.int16) if a.dtype == np.uint16 else a.view(np.int32)
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    set_bytes = w_host.nbytes + inp.scales.nbytes + inp.biases.nbytes
-    R = max(2, int(np.ceil(2.0 * l2 / set_bytes)) + 1)
-    sets = [(tdev(w_host), tdev(inp.scales), tdev(inp.biases)) for _ in range(R)]
-    x_all = tdev(inp.x)
-    stream = torch.cuda.Stream(device=dev)
-    chunk = 500
+    cache = {}
 
-    def measure(M):
-        x = x_all[:M].contiguous()
-        y = torch.empty((M, N), dtype=torch.int16, device=dev)
+    def problem(name):
+        """R rotating device copies of the workload's weights, scales and biases
+        (R * bytes > 2x L2, so every call reads its weights from HBM), and 16
+        activation vectors."""
+        if name not in cache:
+            w = synth.WORKLOADS[name]
+            inp = synth.make_inputs(w["N"], w["K"], 16, w["bits"], w["group_size"], seed=0)
+            w_host = g.qmv_pack(inp.q, w["bits"])
+            set_bytes = w_host.nbytes + inp.scales.nbytes + inp.biases.nbytes
+            R = max(2, int(np.ceil(2.0 * l2 / set_bytes)) + 1)
+            sets = [(tdev(w_host), tdev(inp.scales), tdev(inp.biases)) for _ in range(R)]
+            cache[name] = dict(w, R=R, set_bytes=set_bytes, sets=sets, x=tdev(inp.x), inp=inp)
+        return cache[name]
 
-        def call(i):
-            wq, s, b = sets[i % R]
-            g.qmv_run(wq, s, b, x, y, M, N, K, bits, gs, stream=stream)
-
-        return timed(call, args.steps)
-
-    def timed(call, steps):
-        """`warmup` plain calls, then `steps` calls as graph replays between
-        CUDA events on the launch stream; (job milliseconds, clock summary)."""
+    def timed(call, steps, clocks=False):
+        """`warmup` plain calls; then `steps` calls captured as CUDA graphs of
+        at most CHUNK calls. The timed replays are enqueued right behind
+        untimed replays of at least WARM_CALLS calls, with no host
+        synchronization in between, so the GPU is busy when the start event
+        runs and the host's graph submissions overlap GPU work; the events on
+        the launch stream bracket exactly `steps` calls. Returns (job
+        milliseconds, clock summary or None, timing description)."""
         with torch.cuda.stream(stream):
             for i in range(args.warmup):
                 call(i)
         torch.cuda.synchronize()
-        n_chunks, rem = divmod(steps, chunk)
+        n_chunks, rem = divmod(steps, CHUNK)
         graphs = []
         with torch.cuda.stream(stream):
-            for size in ([chunk] if n_chunks else []) + ([rem] if rem else []):
+            for size in ([CHUNK] if n_chunks else []) + ([rem] if rem else []):
                 gr = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(gr, stream=stream):
                     for i in range(size):
                         call(i)
                 graphs.append(gr)
-            for gr in graphs:  # untimed replay: uploads the graphs
+            for gr in graphs:  # uploads the graphs
                 gr.replay()
         torch.cuda.synchronize()
         big = graphs[0] if n_chunks else None
         tail = graphs[-1] if rem else None
+        warm = big if big is not None else tail
+        warm_reps = max(3, -(-WARM_CALLS // (CHUNK if big is not None else rem)))
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
-        with ClockSampler(local_rank) as clk:
-            with torch.cuda.stream(stream):
-                start.record(stream)
-                for _ in range(n_chunks):
-                    big.replay()
-                if tail is not None:
-                    tail.replay()
-                end.record(stream)
-            torch.cuda.synchronize()
+        clk = ClockSampler(local_rank) if clocks else None
+        if clk:
+            clk.__enter__()
+        with torch.cuda.stream(stream):
+            for _ in range(warm_reps):
+                warm.replay()
+            start.record(stream)
+            for _ in range(n_chunks):
+                big.replay()
+            if tail is not None:
+                tail.replay()
+            end.record(stream)
+        torch.cuda.synchronize()
+        if clk:
+            clk.__exit__(None, None, None)
         if world > 1:
             torch.distributed.barrier()
         ms = max_over_ranks(start.elapsed_time(end), world, dev)
-        return ms, clk.summary()
+        desc = (f"{steps} calls timed as {n_chunks} CUDA-graph replays of {CHUNK} calls"
+                + (f" and one of {rem}" if n_chunks and rem else "" if n_chunks else f" (one replay of {rem})")
+                + f", enqueued behind {warm_reps} untimed replays of the same graph with no host sync between;"
+                  " CUDA events on the launch stream")
+        return ms, (clk.summary() if clk else None), desc
+
+    def measure(name, M, flags=0, steps=None, clocks=False):
+        pr = problem(name)
+        N, K, bits, gs, R, sets = pr["N"], pr["K"], pr["bits"], pr["group_size"], pr["R"], pr["sets"]
+        x = pr["x"][:M].contiguous()
+        y = torch.empty((M, N), dtype=torch.int16, device=dev)
+
+        def call(i):
+            wq, s, b = sets[i % R]
+            if flags:
+                g.qmv_run_ex(wq, s, b, x, y, M, N, K, bits, gs, flags=flags, stream=stream)
+            else:
+                g.qmv_run(wq, s, b, x, y, M, N, K, bits, gs, stream=stream)
+
+        steps = args.steps if steps is None else steps
+        ms, ck, desc = timed(call, steps, clocks)
+        return dict(ms=ms, steps=steps, clocks=ck, timing=desc, N=N, K=K, bits=bits, gs=gs, M=M, R=R,
+                    set_bytes=pr["set_bytes"])
+
+    def measure_stack(M, steps):
+        """One step = the four matrices of the 27B-class layer in turn."""
+        prs = [problem(n) for n in STACK]
+        xs = [pr["x"][:M].contiguous() for pr in prs]
+        ys = [torch.empty((M, pr["N"]), dtype=torch.int16, device=dev) for pr in prs]
+
+        def call(i):
+            for pr, x, y in zip(prs, xs, ys):
+                wq, s, b = pr["sets"][i % pr["R"]]
+                g.qmv_run(wq, s, b, x, y, M, pr["N"], pr["K"], pr["bits"], pr["group_size"], stream=stream)
+
+        ms, _, _ = timed(call, steps)
+        return ms
 
     def measure_e2e(M, steps):
-        x_host = torch.from_numpy(inp.x[:M].view(np.int16).copy()).pin_memory()
+        pr = problem(WORKLOAD)
+        N, K, bits, gs, R, sets = pr["N"], pr["K"], pr["bits"], pr["group_size"], pr["R"], pr["sets"]
+        x_host = torch.from_numpy(pr["inp"].x[:M].view(np.int16).copy()).pin_memory()
         y_host = torch.empty((M, N), dtype=torch.int16).pin_memory()
         x = torch.empty((M, K), dtype=torch.int16, device=dev)
         y = torch.empty((M, N), dtype=torch.int16, device=dev)
@@ -258,8 +313,26 @@ def run_gpu(args, rank, world, local_rank):
         torch.cuda.synchronize()
         return start.elapsed_time(end) / steps, M * K * 2, M * N * 2
 
-    ms1, clocks1 = measure(1)
-    ms13, clocks13 = measure(13)
+    head1 = measure(WORKLOAD, 1, clocks=True)
+    head13 = measure(WORKLOAD, 13, clocks=True)
+
+    # side measurements: the MTP verify sweep on both projection shapes, the
+    # same 13 vectors as 13 one-vector launches, the 27B-class stack, the
+    # 2-bit variants, and the opt-in programmatic-dependency launch
+    xs = min(args.steps, EXTRA_STEPS)
+    sweep = {}
+    for name in (WORKLOAD, "down_3840x15360_4b_g64"):
+        sweep[name] = {M: (head1 if (name == WORKLOAD and M == 1) else head13 if (name == WORKLOAD and M == 13)
+                           else measure(name, M, steps=xs)) for M in SWEEP_MS}
+    per_column = {name: measure(name, 13, flags=g.FORCE_M1_PER_COLUMN, steps=xs)
+                  for name in (WORKLOAD, "down_3840x15360_4b_g64")}
+    stack = {name: {M: measure(name, M, steps=xs) for M in (1, 13)} for name in STACK}
+    stack_step = {M: measure_stack(M, xs) for M in (1, 13)}
+    two_bit = {name: {M: measure(name, M, steps=xs) for M in (1, 13)} for name in TWO_BIT}
+    pdl = measure(WORKLOAD, 1, flags=g.PDL, steps=xs)
+    for name in list(cache):
+        if name != WORKLOAD:
+            del cache[name]
 
     # the mxfp4 mode on the same projection shape
     mxw = synth.MX_WORKLOADS[MX_WORKLOAD]
@@ -279,18 +352,66 @@ def run_gpu(args, rank, world, local_rank):
             wq, sc = msets[i % mR]
             g.qmv_mxfp4_run(wq, sc, x, y, M, mN, mK, stream=stream)
 
-        return timed(call, mx_steps)
+        return timed(call, mx_steps, clocks=(M == 13))
 
-    mx_ms1, _ = measure_mx(1)
-    mx_ms13, mx_clocks13 = measure_mx(13)
+    mx_ms1, _, _ = measure_mx(1)
+    mx_ms13, mx_clocks13, _ = measure_mx(13)
     del msets
     e2e_steps = min(args.steps, 3000)
     e2e_ms, h2d, d2h = measure_e2e(1, e2e_steps)
-    return dict(N=N, K=K, bits=bits, gs=gs, R=R, set_bytes=set_bytes, l2=l2, ms1=ms1, ms13=ms13, clocks1=clocks1,
-                clocks13=clocks13, e2e_ms=e2e_ms, e2e_steps=e2e_steps, h2d=h2d, d2h=d2h,
+    pr = problem(WORKLOAD)
+    return dict(N=pr["N"], K=pr["K"], bits=pr["bits"], gs=pr["group_size"], R=pr["R"], set_bytes=pr["set_bytes"],
+                l2=l2, ms1=head1["ms"], ms13=head13["ms"], clocks1=head1["clocks"], clocks13=head13["clocks"],
+                timing=head1["timing"], e2e_ms=e2e_ms, e2e_steps=e2e_steps, h2d=h2d, d2h=d2h,
+                sweep=sweep, per_column=per_column, stack=stack, stack_step=stack_step, two_bit=two_bit, pdl=pdl,
+                extra_steps=xs,
                 mx=dict(N=mN, K=mK, R=mR, set_bytes=mset_bytes, steps=mx_steps, ms1=mx_ms1, ms13=mx_ms13,
                         clocks13=mx_clocks13),
                 sm_count=torch.cuda.get_device_properties(dev).multi_processor_count)
+
+
+def call_summary(m, peak, fma_peak_tflops):
+    """µs per call, GB/s and fractions of one side measurement."""
+    us = m["ms"] * 1e3 / m["steps"]
+    nbytes = algorithmic_bytes(m["N"], m["K"], m["M"], m["bits"], m["gs"])
+    gbs = nbytes / (us * 1e-6) / 1e9
+    d = {"us_per_call": round(us, 3), "achieved_gbs": round(gbs, 2), "hbm_frac": round(gbs / peak, 4)}
+    if m["M"] > 1:
+        tflops = 2.0 * m["N"] * m["K"] * m["M"] / (us * 1e-6) / 1e12
+        d.update(fp32_tflops=round(tflops, 2), fp32_frac=round(tflops / fma_peak_tflops, 4))
+    return d
+
+
+def side_summary(r, peak, fma_peak_tflops):
+    """The extra objects of the bench line (issue #1289 "Step 1" and
+    "Acceptance criteria": the verify sweep and the recovered gap; PR #1681
+    "What lands": the 27B-class stack; PR #159 "What": 2-bit, groups 64/128)."""
+    us = lambda m: m["ms"] * 1e3 / m["steps"]
+    sweep = {}
+    for name, by_m in r["sweep"].items():
+        t1 = us(by_m[1])
+        sweep[name] = {f"m{M}": dict(call_summary(m, peak, fma_peak_tflops), ratio_to_m1=round(us(m) / t1, 3))
+                       for M, m in by_m.items()}
+    gap = {}
+    for name, pc in r["per_column"].items():
+        t_stream, t1, t_pc = us(r["sweep"][name][13]), us(r["sweep"][name][1]), us(pc)
+        gap[name] = {"m13_streamed_us": round(t_stream, 3), "m13_as_13_launches_us": round(t_pc, 3),
+                     "m1_us": round(t1, 3), "speedup_vs_13_launches": round(t_pc / t_stream, 3),
+                     "recovered_frac": round((t_pc - t_stream) / (t_pc - t1), 4) if t_pc > t1 else None}
+    stack = {name: {f"m{M}": call_summary(m, peak, fma_peak_tflops) for M, m in by_m.items()}
+             for name, by_m in r["stack"].items()}
+    for M, ms in r["stack_step"].items():
+        nbytes = sum(algorithmic_bytes(r["stack"][n][M]["N"], r["stack"][n][M]["K"], M, 4, 64) for n in STACK)
+        t = ms * 1e3 / r["extra_steps"]
+        stack[f"stack_m{M}"] = {"us_per_step": round(t, 3), "bytes_per_step": nbytes,
+                                "achieved_gbs": round(nbytes / (t * 1e-6) / 1e9, 2),
+                                "hbm_frac": round(nbytes / (t * 1e-6) / 1e9 / peak, 4)}
+    two_bit = {name: {f"m{M}": call_summary(m, peak, fma_peak_tflops) for M, m in by_m.items()}
+               for name, by_m in r["two_bit"].items()}
+    pdl = dict(call_summary(r["pdl"], peak, fma_peak_tflops),
+               note="QMV_PDL (opt-in): each call may start streaming weights under the previous call's tail")
+    return {"steps_each": r["extra_steps"], "mtp_sweep": sweep, "recovered_gap": gap, "stack_27b": stack,
+            "two_bit": two_bit, "pdl_m1": pdl}
 
 
 # --------------------------------------------------------------------------- CPU oracle
@@ -508,7 +629,7 @@ def main():
             "config": {"workload": WORKLOAD, "N": N, "K": K, "M": 1, "bits": bits, "group_size": gs,
                        "l2": f"inputs > L2: {r['R']} rotating weight copies of {r['set_bytes'] / 1e6:.1f} MB "
                              f"({r['R'] * r['set_bytes'] / 1e6:.0f} MB) vs L2 {r['l2'] / 1e6:.0f} MB",
-                       "timing": "CUDA-graph replays of 500 calls, CUDA events on the launch stream",
+                       "timing": r["timing"],
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "us_per_call": round(us1, 3),
             "roofline": {"bound": "hbm", "achieved": round(gbs1, 2), "peak": peak, "unit": "GB/s",
@@ -523,6 +644,7 @@ def main():
                     "fp32_frac": round(flops13 / (us13 * 1e-6) / 1e12 / fma_peak_tflops, 4),
                     "kernel": "qmv_streamed<4,64,13>", "bytes_per_launch": b13, "clocks": r["clocks13"]},
             "mxfp4": mx_summary(r["mx"], peak, fma_peak_tflops, cpu=(256, *mx_oracle_timing(r["mx"]["K"]))),
+            "side": side_summary(r, peak, fma_peak_tflops),
             "clocks": r["clocks1"],
             "e2e": {"value": round(world * e2e_gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
                     "d2h_bytes_per_step": r["d2h"], "us_per_step": round(r["e2e_ms"] * 1e3, 3),

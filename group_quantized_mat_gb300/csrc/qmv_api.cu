@@ -82,11 +82,6 @@ constexpr int kXsBudgetV1 = 100 * 1024;
 constexpr int kUnitMax = 8 * 1024;
 constexpr int kMaxSlots = 24;
 
-#if defined(QMV_TUNING)
-// Tuning builds only: fixed launch shapes for sweeps (0 = automatic).
-struct TuneOverride { int slots = 0, uc = 0, consumers = 0, grid_rows = 0, cpc = 0; };
-TuneOverride g_tune;
-#endif
 
 void common_shape(Problem &pr, int V, int N, int K, int bits, int gs)
 {
@@ -110,9 +105,6 @@ void grid_shape(Problem &pr, int sms, int V, int cv_bytes)
     const int rb_cap = cv_bytes / per_rb > 0 ? cv_bytes / per_rb : 1;
     if ((pr.NB + gr - 1) / gr > rb_cap) gr = (pr.NB + rb_cap - 1) / rb_cap;
     if (gr > pr.NB) gr = pr.NB;
-#if defined(QMV_TUNING)
-    if (g_tune.grid_rows > 0) gr = g_tune.grid_rows < pr.NB ? g_tune.grid_rows : pr.NB;
-#endif
     pr.grid_rows = gr;
     pr.max_rb = (pr.NB + gr - 1) / gr;
 }
@@ -131,9 +123,6 @@ Problem plan_direct(int V, int N, int K, int bits, int gs, int sms)
     auto xs_bytes = [&](int cpc) { return qmv::align_up(V * nsub_of(cpc) * qmv::kXsF32, 16); };
     pr.cpc = pr.ks;
     while (pr.cpc > 1 && xs_bytes(pr.cpc) + kCvBudget + wbuf + 16 + 128 > kSmemBudget) --pr.cpc;
-#if defined(QMV_TUNING)
-    if (g_tune.cpc > 0 && g_tune.cpc <= pr.ks) pr.cpc = g_tune.cpc;
-#endif
     pr.threads = 32 * warps;
     // chunk values may use whatever shared memory the x cells and the weight
     // buffer leave (at least kCvBudget, by the fit above)
@@ -155,16 +144,9 @@ Problem plan_ring(int N, int K, int bits, int gs, int sms, bool sb_packed)
     const int per_chunk = qmv::kChunkSubs * qmv::kXsB16;
     pr.cpc = pr.S_row * qmv::kXsB16 <= kXsBudgetV1 ? pr.ks : kXsBudgetV1 / per_chunk;
     pr.consumers = qmv::kRingConsumers;
-#if defined(QMV_TUNING)
-    if (g_tune.cpc > 0 && g_tune.cpc <= pr.ks) pr.cpc = g_tune.cpc;
-    if (g_tune.consumers > 0 && g_tune.consumers <= qmv::kRingConsumers) pr.consumers = g_tune.consumers;
-#endif
     grid_shape(pr, sms, 1, kCvBudget);
     const int cb = qmv::chunk_bytes(bits);
     bool whole = pr.cpc == pr.ks && qmv::kRows * pr.row_bytes <= kUnitMax;
-#if defined(QMV_TUNING)
-    if (g_tune.uc > 0) whole = false;
-#endif
     if (whole) {
         pr.unit_mode = qmv::kUnitRows;
         pr.uc = pr.ks;
@@ -175,9 +157,6 @@ Problem plan_ring(int N, int K, int bits, int gs, int sms, bool sb_packed)
         pr.uc = kUnitMax / (qmv::kRows * cb);
         if (pr.uc < 1) pr.uc = 1;
         if (pr.uc > pr.cpc) pr.uc = pr.cpc;
-#if defined(QMV_TUNING)
-        if (g_tune.uc > 0 && g_tune.uc <= pr.cpc) pr.uc = g_tune.uc;
-#endif
         pr.pitch = pr.uc * cb;
     }
     // Scale/bias boxes: one per unit when the four rows' groups fit one box,
@@ -205,9 +184,6 @@ Problem plan_ring(int N, int K, int bits, int gs, int sms, bool sb_packed)
     const int upr = (pr.cpc + pr.uc - 1) / pr.uc;
     const int units = pr.max_rb * upr;
     int slots = kMaxSlots < units ? kMaxSlots : units;
-#if defined(QMV_TUNING)
-    if (g_tune.slots >= 2) slots = g_tune.slots;
-#endif
     const int P = qmv::kRingProducers;
     slots = (slots + P - 1) / P * P;
     while (slots > P && layout(slots).total > kSmemBudget) slots -= P;
@@ -329,7 +305,10 @@ qmv_status device_error_ptr(int dev, unsigned **out)
     return QMV_OK;
 }
 
-// Library-owned workspace of `dev`, grown (and zero-filled) on demand.
+// Library-owned workspace of `dev`, grown on demand. It is scratch (every
+// launch clears the tickets it uses on its own stream), so a new allocation
+// needs no initialization. Growing frees the smaller one first: cudaFree
+// waits for the device's work in flight, which may still be using it.
 qmv_status library_workspace(int dev, size_t need, void **out)
 {
     std::lock_guard<std::mutex> lock(g_mutex);
@@ -343,12 +322,6 @@ qmv_status library_workspace(int dev, size_t need, void **out)
         void *p = nullptr;
         cudaError_t e = cudaMalloc(&p, need);
         if (e != cudaSuccess) return cuda_fail("cudaMalloc(workspace)", e);
-        e = cudaMemset(p, 0, need);
-        if (e == cudaSuccess) e = cudaDeviceSynchronize();
-        if (e != cudaSuccess) {
-            cudaFree(p);
-            return cuda_fail("cudaMemset(workspace)", e);
-        }
         d.workspace = p;
         d.workspace_bytes = need;
     }
@@ -404,9 +377,14 @@ cudaError_t dispatch(const Problem &pr, const qmv::RingMaps &maps, const qmv::Pa
     return qmv::launch_b2g128_streamed(pr.V, p, l, stream);
 }
 
-qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t *biases, const uint16_t *x, void *y,
-                    int M, int N, int K, int bits, int gs, void *workspace, size_t workspace_bytes, unsigned flags,
-                    cudaStream_t stream)
+}  // namespace
+
+namespace qmv {
+
+// The host-side argument checks of a qmv_run_ex call, in the order they are
+// reported: pointers, shape, flags, alignment.
+qmv_status check_run_args(const void *w_q, const void *scales, const void *biases, const void *x, const void *y,
+                          int M, int N, int K, int bits, int gs, const void *workspace, unsigned flags)
 {
     const bool sb_packed = (flags & QMV_SB_INTERLEAVED) != 0;
     if (!w_q || !scales || (!biases && !sb_packed) || !x || !y) return QMV_ERR_NULL;
@@ -417,6 +395,23 @@ qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t 
     if (!aligned(w_q, 16) || !aligned(x, 16) || !aligned(scales, 16) || (!sb_packed && !aligned(biases, 16)) ||
         !aligned(y, f32_out ? 4 : 2) || (workspace && !aligned(workspace, 16)))
         return QMV_ERR_ALIGN;
+    return QMV_OK;
+}
+
+qmv_status record_cuda_failure(const char *what, cudaError_t e) { return cuda_fail(what, e); }
+
+}  // namespace qmv
+
+namespace {
+
+qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t *biases, const uint16_t *x, void *y,
+                    int M, int N, int K, int bits, int gs, void *workspace, size_t workspace_bytes, unsigned flags,
+                    cudaStream_t stream)
+{
+    qmv_status st = qmv::check_run_args(w_q, scales, biases, x, y, M, N, K, bits, gs, workspace, flags);
+    if (st != QMV_OK) return st;
+    const bool sb_packed = (flags & QMV_SB_INTERLEAVED) != 0;
+    const bool f32_out = (flags & QMV_F32_OUT) != 0;
 
     static_assert(qmv::kMaxM == QMV_TILE_M, "launch width");
     // Vectors go through in launches of at most kMaxM (one each with
@@ -508,17 +503,6 @@ extern "C" int qmv_split_count(int N, int K, int bits, int group_size)
     return qmv::chunk_count(K);
 }
 
-#if defined(QMV_TUNING)
-extern "C" __attribute__((visibility("default"))) void qmv_tune_set(int slots, int uc, int consumers, int grid_rows,
-                                                                     int cpc)
-{
-    g_tune.slots = slots;
-    g_tune.uc = uc;
-    g_tune.consumers = consumers;
-    g_tune.grid_rows = grid_rows;
-    g_tune.cpc = cpc;
-}
-#endif
 
 extern "C" size_t qmv_workspace_size(int M, int N, int K, int bits, int group_size)
 {

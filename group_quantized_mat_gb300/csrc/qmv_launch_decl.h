@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "qmv.h"
 #include "qmv_plan.h"
 
 namespace qmv {
@@ -35,6 +36,13 @@ struct MxParams {
     int N, K;                // K a multiple of 32
     int f32_out;
 };
+
+// Host-side argument checks of qmv_run_ex (QMV_OK or the status it would
+// return, nothing launched), and recording a CUDA failure as the calling
+// thread's qmv_last_cuda_error() text (returns QMV_ERR_CUDA). qmv_api.cu.
+qmv_status check_run_args(const void *w_q, const void *scales, const void *biases, const void *x, const void *y,
+                          int M, int N, int K, int bits, int gs, const void *workspace, unsigned flags);
+qmv_status record_cuda_failure(const char *what, cudaError_t e);
 
 // One launch for V = 1..16 vectors (qmv_mx.cu).
 cudaError_t launch_mxfp4(int V, const MxParams &p, cudaStream_t stream);

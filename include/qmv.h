@@ -139,13 +139,18 @@ QMV_API size_t qmv_workspace_size(int M, int N, int K, int bits, int group_size)
  * an M-vector call is bit-identical to an M = 1 call on x[j] (issue #1289
  * "The observation this rests on": "bit-identical ... by construction").
  *
- * The call returns after enqueueing; it never synchronizes. A problem with
- * more than one K-split needs scratch: qmv_run uses a workspace owned by the
- * library, one per device, allocated (cudaMalloc) on the first call that needs
- * more than the current one and kept until exit. That first call is not
- * stream-ordered and must not be made during stream capture; calls that share
- * the library workspace must not overlap on the GPU (use qmv_run_ex with
- * separate workspaces for concurrent streams).
+ * The call returns after enqueueing. Most calls need no scratch (M = 1 with
+ * the whole of K per CTA); M >= 2, and problems whose CTAs split K, need a
+ * workspace (qmv_workspace_size). qmv_run then uses one owned by the library,
+ * one per device, kept until exit. The first call that needs more than the
+ * current one allocates it with cudaMalloc (after cudaFree of the smaller one,
+ * which waits for the device's work in flight): that call is not stream-ordered,
+ * may block the host until the device is idle, and must not be made during
+ * stream capture. No other qmv_run call allocates or synchronizes. Every call
+ * on a device shares the one library workspace, so qmv_run calls that overlap
+ * on the GPU (issued to different streams, or from concurrent host threads)
+ * race on it and give undefined results: concurrent callers use qmv_run_ex
+ * with one workspace each, or serialize their calls on one stream.
  *
  * Errors: QMV_ERR_NULL, QMV_ERR_BITS, QMV_ERR_GROUP, QMV_ERR_SHAPE,
  * QMV_ERR_M_RANGE, QMV_ERR_ALIGN (host checks, nothing launched);
@@ -205,12 +210,14 @@ QMV_API qmv_status qmv_run_ex(const uint32_t *w_q, const uint16_t *scales, const
  * calls that overlap on the GPU (other streams, or concurrent host threads)
  * race and give undefined results.
  *
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.
+ * The first call on a device, whatever its shape, looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture.
  *
- * Errors: as qmv_run, plus QMV_ERR_WORKSPACE when the problem's
- * qmv_workspace_size() exceeds QMV_NOALLOC_SCRATCH_BYTES (nothing launched). */
+ * Errors: those of qmv_run, checked first and in the same order; then
+ * QMV_ERR_WORKSPACE when the problem's qmv_workspace_size() exceeds
+ * QMV_NOALLOC_SCRATCH_BYTES (nothing launched); QMV_ERR_CUDA when the address
+ * lookup or a launch fails (qmv_last_cuda_error() says which). */
 QMV_API qmv_status qmv_run_noalloc(const uint32_t *w_q, const uint16_t *scales, const uint16_t *biases,
                                    const uint16_t *x, uint16_t *y, int M, int N, int K, int bits,
                                    int group_size, qmv_stream_t stream);

@@ -3,6 +3,9 @@ the C ABI, and oracle references for selected rows."""
 
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import torch
 
@@ -55,16 +58,39 @@ class DeviceProblem:
         return out if f32 else out.view(np.uint16)
 
 
+def row_slices(n: int, parts: int):
+    """[lo, hi) bounds splitting n rows into at most `parts` contiguous slices."""
+    step = max(1, -(-n // parts))
+    return [(lo, min(n, lo + step)) for lo in range(0, n, step)]
+
+
+def threaded_rows(fn, n: int, M: int, threads: int | None = None) -> np.ndarray:
+    """fn(lo, hi) -> [M, hi - lo] evaluated over row slices on a thread pool
+    (the oracle's C calls release the GIL) and joined along the rows. Rows are
+    independent outputs, so slicing changes no value."""
+    threads = threads or min(16, os.cpu_count() or 1)
+    parts = row_slices(n, threads)
+    out = np.empty((M, n), dtype=np.float64)
+    with ThreadPoolExecutor(max_workers=len(parts)) as ex:
+        for (lo, hi), blk in zip(parts, ex.map(lambda b: fn(*b), parts)):
+            out[:, lo:hi] = blk
+    return out
+
+
 def oracle_rows(o: Oracle, inp: synth.QmvInputs, rows: np.ndarray | None = None):
     """fp64 reference y and sum|w x| for the given rows (all rows when None),
-    computed from the oracle's own packing of q."""
+    computed from the oracle's own packing of q; large problems are split
+    over host threads by rows."""
     pr = inp.problem
     q = inp.q if rows is None else inp.q[rows]
     s = inp.scales if rows is None else inp.scales[rows]
     b = inp.biases if rows is None else inp.biases[rows]
     w = o.pack(q, pr.bits)
-    y = o.qmv_f64_dequant(w, s, b, inp.x, pr.bits, pr.group_size)
-    t = o.abs_terms(w, s, b, inp.x, pr.bits, pr.group_size)
+    n, M = w.shape[0], np.atleast_2d(inp.x).shape[0]
+    y = threaded_rows(lambda lo, hi: o.qmv_f64_dequant(w[lo:hi], s[lo:hi], b[lo:hi], inp.x, pr.bits,
+                                                       pr.group_size), n, M)
+    t = threaded_rows(lambda lo, hi: o.abs_terms(w[lo:hi], s[lo:hi], b[lo:hi], inp.x, pr.bits, pr.group_size),
+                      n, M)
     return y, t
 
 

@@ -14,7 +14,7 @@ import torch
 
 import group_quantized_mat_gb300 as g
 import synth
-from gpu_helpers import dev
+from gpu_helpers import dev, threaded_rows
 from oracle import Oracle, tolerance_ok
 
 pytestmark = pytest.mark.gpu
@@ -164,16 +164,16 @@ def test_mxfp4_one_hot_x_reads_single_weights(o):
 
 
 @pytest.mark.parametrize("N,K,M", [(15360, 3840, 1), (15360, 3840, 13), (3840, 15360, 13)])
-def test_mxfp4_full_size_sampled_rows(o, N, K, M):
-    """The bench's shapes, checked on sampled rows (the oracle computes each one
-    alone) including the first and the last."""
+def test_mxfp4_full_size_all_rows(o, N, K, M):
+    """The bench's shapes: every output element against the oracle (computed
+    over row slices on host threads)."""
     inp = synth.make_mxfp4_inputs(N, K, M, seed=21)
     d = MxDevice(inp)
     y = d.run()
-    rng = np.random.default_rng(5)
-    rows = np.unique(np.concatenate([[0, 31, 32, N - 1], rng.choice(N, 96, replace=False)]))
-    y_ref, terms = oracle_rows(o, inp, rows=rows)
-    check(y[:, rows], y_ref, terms, f"mxfp4 {N}x{K} M={M} sampled")
+    w = o.pack(inp.codes, 4)
+    y_ref = threaded_rows(lambda lo, hi: o.mxfp4_qmv_f64(w[lo:hi], inp.scales[lo:hi], inp.x), N, M)
+    terms = threaded_rows(lambda lo, hi: o.mxfp4_abs_terms(w[lo:hi], inp.scales[lo:hi], inp.x), N, M)
+    check(y, y_ref, terms, f"mxfp4 {N}x{K} M={M}")
 
 
 @pytest.mark.parametrize("M", [1, 3])

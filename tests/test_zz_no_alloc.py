@@ -27,11 +27,18 @@ def lib():
     return g.load()
 
 
-def test_noalloc_matches_existing_entry_point_twice(lib):
-    N, K, M, bits, gs = 3840, 15360, 13, 4, 64
+# (N, K, M): the streamed kernel with a K split; a one-vector launch whose
+# CTAs split K (its tickets live in the array and are cleared on the stream);
+# more than 16 vectors, which run as two launches sharing the array.
+CASES = [(3840, 15360, 13), (64, 65536, 1), (3840, 15360, 17)]
+
+
+@pytest.mark.parametrize("N,K,M", CASES)
+def test_noalloc_matches_existing_entry_point_twice(lib, N, K, M):
+    bits, gs = 4, 64
     need = g.qmv_workspace_size(M, N, K, bits, gs)
-    assert 0 < need <= g.NOALLOC_SCRATCH_BYTES  # this problem uses K-split scratch
-    inp = synth.make_inputs(N, K, M, bits, gs, seed=41)
+    assert 0 < need <= g.NOALLOC_SCRATCH_BYTES  # this problem uses scratch
+    inp = synth.make_inputs(N, K, M, bits, gs, seed=41 + M)
     dp = DeviceProblem(inp)
 
     ws = torch.zeros(need // 4 + 4, dtype=torch.int32, device="cuda")
@@ -40,22 +47,28 @@ def test_noalloc_matches_existing_entry_point_twice(lib):
     torch.cuda.synchronize()
     ref_bits = ref.cpu().numpy().view(np.uint16)
 
-    rows = np.unique(np.concatenate([np.random.default_rng(5).choice(N, 64, replace=False), [0, N - 1]]))
+    rows = np.unique(np.concatenate([np.random.default_rng(5).choice(N, min(N, 64), replace=False), [0, N - 1]]))
     _, terms = oracle_rows(Oracle(0), inp, rows)
     y_ref = synth.bf16_bits_to_f32(ref_bits).astype(np.float64)
 
-    for call in range(2):
-        y = torch.full((M, N), -1, dtype=torch.int16, device="cuda")
+    outs = [torch.full((M, N), -1, dtype=torch.int16, device="cuda") for _ in range(2)]
+    torch.cuda.synchronize()
+    free_before = None
+    for call, y in enumerate(outs):
         code = lib.qmv_run_noalloc(dp.w.data_ptr(), dp.s.data_ptr(), dp.b.data_ptr(), dp.x.data_ptr(),
                                    y.data_ptr(), M, N, K, bits, gs, torch.cuda.current_stream().cuda_stream)
         assert code == 0, g.qmv_status_string(code)
         torch.cuda.synchronize()
+        if call == 0:
+            # the first call may load the kernels; the next one adds nothing
+            free_before = torch.cuda.mem_get_info()[0]
         got_bits = y.cpu().numpy().view(np.uint16)
         got = synth.bf16_bits_to_f32(got_bits).astype(np.float64)
         # within the acceptance tolerance of the existing entry point's output ...
         assert np.all(np.abs(got[:, rows] - y_ref[:, rows]) <= 8e-3 * terms + 1e-5), f"call {call}"
         # ... and, since the arithmetic is the same, bit for bit
         assert np.array_equal(got_bits, ref_bits), f"call {call}"
+    assert torch.cuda.mem_get_info()[0] == free_before, "a call took device memory"
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(lib):
