@@ -78,9 +78,11 @@ constexpr int kSmemBudget = 227 * 1024 - 512;
 // Chunk values of one CTA at most (bounds its share of rows).
 constexpr int kCvBudget = 16 * 1024;
 // One-vector kernel: staged x at most, largest unit, ring depth.
-constexpr int kXsBudgetV1 = 100 * 1024;
+constexpr int kXsBudgetV1 = 80 * 1024;
 constexpr int kUnitMax = 8 * 1024;
-constexpr int kMaxSlots = 24;
+constexpr int kMaxSlots = 32;
+// Rows at least this long go to the ring whatever their unit shape.
+constexpr int kRingMinK = 12288;
 
 
 void common_shape(Problem &pr, int V, int N, int K, int bits, int gs)
@@ -141,8 +143,9 @@ Problem plan_ring(int N, int K, int bits, int gs, int sms, bool sb_packed)
 {
     Problem pr{};
     common_shape(pr, 1, N, K, bits, gs);
-    const int per_chunk = qmv::kChunkSubs * qmv::kXsB16;
-    pr.cpc = pr.S_row * qmv::kXsB16 <= kXsBudgetV1 ? pr.ks : kXsBudgetV1 / per_chunk;
+    // raw x (128 bytes a subgroup) and its staged cell (kXsB16 bytes)
+    const int per_sub = 128 + qmv::kXsB16;
+    pr.cpc = pr.S_row * per_sub <= kXsBudgetV1 ? pr.ks : kXsBudgetV1 / (qmv::kChunkSubs * per_sub);
     pr.consumers = qmv::kRingConsumers;
     grid_shape(pr, sms, 1, kCvBudget);
     const int cb = qmv::chunk_bytes(bits);
@@ -181,22 +184,52 @@ Problem plan_ring(int N, int K, int bits, int gs, int sms, bool sb_packed)
     auto layout = [&](int slots) {
         return qmv::ring_layout(pr.pitch, pr.sb_mode_unit, pr.sbox, pr.sb_packed, slots, nsub, pr.max_rb, pr.cpc);
     };
-    const int upr = (pr.cpc + pr.uc - 1) / pr.uc;
-    const int units = pr.max_rb * upr;
-    int slots = kMaxSlots < units ? kMaxSlots : units;
+    // Slots: a multiple of the producer and the consumer counts (each slot
+    // has one producer and one consumer warp); fewer consumer warps when the
+    // ring of one slot per consumer does not fit.
     const int P = qmv::kRingProducers;
-    slots = (slots + P - 1) / P * P;
-    while (slots > P && layout(slots).total > kSmemBudget) slots -= P;
+    int C = qmv::kRingConsumers;
+    while (C > P && layout(C).total > kSmemBudget) C /= 2;
+    int slots = C;
+    while (slots + C <= kMaxSlots && layout(slots + C).total <= kSmemBudget) slots += C;
+    pr.consumers = C;
     pr.slots = slots;
     pr.smem = layout(slots).total;
-    if (pr.consumers > pr.slots) pr.consumers = pr.slots;  // at most one consumer warp per slot
-    pr.threads = 32 * (pr.consumers + P);
+    pr.threads = 32 * (C + P);
+    return pr;
+}
+
+// One-vector kernel qmv_one: all of K per CTA when its staged x fits the
+// budget, else the widest chunk range that does; about kOneCtasPerSm CTAs per
+// SM. Like plan_direct, the K split never depends on `sms`.
+constexpr int kUnitOne = -1;  // unit_mode of a qmv_one plan
+constexpr int kXsBudgetOne = 48 * 1024;
+constexpr int kCvBudgetOne = 8 * 1024;
+
+Problem plan_one(int N, int K, int bits, int gs, int sms, bool sb_packed)
+{
+    Problem pr{};
+    common_shape(pr, 1, N, K, bits, gs);
+    const int per_chunk = qmv::kChunkSubs * qmv::kXsB16;
+    pr.cpc = pr.S_row * qmv::kXsB16 <= kXsBudgetOne ? pr.ks : kXsBudgetOne / per_chunk;
+    grid_shape(pr, sms * qmv::kOneCtasPerSmDecl, 1, kCvBudgetOne);
+    pr.threads = 32 * qmv::kOneWarpsDecl;
+    const int nsub = pr.cpc * qmv::kChunkSubs < pr.S_row ? pr.cpc * qmv::kChunkSubs : pr.S_row;
+    pr.smem = qmv::one_layout(nsub, pr.max_rb, pr.cpc).total;
+    pr.unit_mode = kUnitOne;
+    pr.sb_packed = sb_packed ? 1 : 0;
     return pr;
 }
 
 Problem plan(int V, int N, int K, int bits, int gs, int sms, bool sb_packed = false)
 {
-    return V == 1 ? plan_ring(N, K, bits, gs, sms, sb_packed) : plan_direct(V, N, K, bits, gs, sms);
+    if (V >= 2) return plan_direct(V, N, K, bits, gs, sms);
+    // One vector: the ring when a unit is four whole rows in one copy, or
+    // for long rows (where staging x once per SM, not per CTA, matters);
+    // otherwise the direct-load kernel, whose units need no per-row copies.
+    const long long four_rows = (long long)qmv::kRows * K * bits / 8;
+    if (four_rows <= kUnitMax || K >= kRingMinK) return plan_ring(N, K, bits, gs, sms, sb_packed);
+    return plan_one(N, K, bits, gs, sms, sb_packed);
 }
 
 size_t counter_bytes(int NB) { return (size_t(NB) * sizeof(unsigned) + 255) & ~size_t(255); }
@@ -361,6 +394,12 @@ cudaError_t dispatch(const Problem &pr, const qmv::RingMaps &maps, const qmv::Pa
         cudaError_t e = cudaMemsetAsync(p.counters, 0, counter_bytes(pr.NB), stream);
         if (e != cudaSuccess) return e;
     }
+    if (pr.V == 1 && pr.unit_mode == kUnitOne) {
+        if (pr.bits == 4 && pr.gs == 64) return qmv::launch_b4g64_one(p, l, stream);
+        if (pr.bits == 4 && pr.gs == 128) return qmv::launch_b4g128_one(p, l, stream);
+        if (pr.bits == 2 && pr.gs == 64) return qmv::launch_b2g64_one(p, l, stream);
+        return qmv::launch_b2g128_one(p, l, stream);
+    }
     if (pr.V == 1) {
         qmv::RingParams rp;
         static_cast<qmv::Params &>(rp) = p;
@@ -461,7 +500,7 @@ qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t 
 
         qmv::RingMaps maps;
         memset(&maps, 0, sizeof maps);
-        if (V == 1) {
+        if (V == 1 && pr.unit_mode != kUnitOne) {
             int enc = encode_sb_map(&maps.s, scales, pr);
             if (enc == 0 && !sb_packed) enc = encode_sb_map(&maps.b, biases, pr);
             if (enc == 0 && pr.unit_mode == qmv::kUnitTiles) enc = encode_w_map(&maps.w, w_q, pr);

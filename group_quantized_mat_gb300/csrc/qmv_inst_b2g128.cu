@@ -6,6 +6,10 @@ cudaError_t launch_b2g128_m1(const RingMaps &maps, const RingParams &p, const La
 {
     return launch_m1<2, 128>(maps, p, l, stream);
 }
+cudaError_t launch_b2g128_one(const Params &p, const Launch &l, cudaStream_t stream)
+{
+    return launch_one_vector<2, 128>(p, l, stream);
+}
 cudaError_t launch_b2g128_streamed(int V, const Params &p, const Launch &l, cudaStream_t stream)
 {
     return launch_streamed<2, 128>(V, p, l, stream);

@@ -6,6 +6,10 @@ cudaError_t launch_b2g64_m1(const RingMaps &maps, const RingParams &p, const Lau
 {
     return launch_m1<2, 64>(maps, p, l, stream);
 }
+cudaError_t launch_b2g64_one(const Params &p, const Launch &l, cudaStream_t stream)
+{
+    return launch_one_vector<2, 64>(p, l, stream);
+}
 cudaError_t launch_b2g64_streamed(int V, const Params &p, const Launch &l, cudaStream_t stream)
 {
     return launch_streamed<2, 64>(V, p, l, stream);

@@ -139,25 +139,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     return false;
 }
 
-// Bounded wait until a producer's issued-unit count passes unit u.
-__device__ __forceinline__ bool wait_issued(volatile int *count, int u)
-{
-    if (*count > u) {
-        __threadfence_block();
-        return true;
-    }
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 0; it < (1u << 24); ++it) {
-        __nanosleep(32);
-        if (*count > u) {
-            __threadfence_block();
-            return true;
-        }
-        if (global_timer_ns() - t0 > 2000000000ull) return false;
-    }
-    return false;
-}
-
 __device__ __forceinline__ uint64_t l2_evict_first_policy()
 {
     uint64_t pol;
@@ -379,16 +360,18 @@ __device__ __forceinline__ void piece_offsets(int lane, uint32_t (&off)[BITS == 
 // two halves of w & 0x000F000F, w & 0x00F000F0 and the same masks of w >> 8.
 // A 2-bit word holds octets 2p (low halves) and 2p + 1 (high halves): fields
 // k and k + 4 of both in the masks 3 << 2k of w and of w >> 8.
-template <int BITS>
+//   SWZ       false: octet o at xsub + 16 * o instead (no swizzle).
+template <int BITS, bool SWZ = true>
 __device__ __forceinline__ void subgroup_dot_v1(const uint4 (&quads)[kRows][BITS == 4 ? 2 : 1], uint32_t xsub, uint32_t sw,
                                                 float (&ae)[kRows], float (&ao)[kRows])
 {
+    auto oct = [&](int o) { return SWZ ? xsub + ((uint32_t(o) ^ sw) << 4) : xsub + (uint32_t(o) << 4); };
 #pragma unroll
     for (int r = 0; r < kRows; ++r) ae[r] = ao[r] = 0.0f;
     if constexpr (BITS == 4) {
 #pragma unroll
         for (int o = 0; o < 8; ++o) {
-            const uint4 X = lds_v4_u32(xsub + ((uint32_t(o) ^ sw) << 4));
+            const uint4 X = lds_v4_u32(oct(o));
 #pragma unroll
             for (int r = 0; r < kRows; ++r) {
                 const uint32_t w = word_of(quads[r][o >> 2], o & 3), w8 = w >> 8;
@@ -407,8 +390,8 @@ __device__ __forceinline__ void subgroup_dot_v1(const uint4 (&quads)[kRows][BITS
     } else {
 #pragma unroll
         for (int pw = 0; pw < 4; ++pw) {
-            const uint4 X0 = lds_v4_u32(xsub + ((uint32_t(2 * pw) ^ sw) << 4));
-            const uint4 X1 = lds_v4_u32(xsub + ((uint32_t(2 * pw + 1) ^ sw) << 4));
+            const uint4 X0 = lds_v4_u32(oct(2 * pw));
+            const uint4 X1 = lds_v4_u32(oct(2 * pw + 1));
 #pragma unroll
             for (int r = 0; r < kRows; ++r) {
                 const uint32_t w = word_of(quads[r][0], pw), w8 = w >> 8;
@@ -660,32 +643,30 @@ __device__ __forceinline__ void stage_all_body(const uint16_t *x, int K, int S_r
     if (live) write_cell<BITS>(out + (size_t(v) * S_row + t) * kXsF32, t, e8, packed, meta);
 }
 
-// Stages x (one vector) for the one-vector kernel in place: the raw bf16 x of
-// subgroups [sub_lo, sub_lo + nsub) lies densely at xs (128 bytes a
-// subgroup); subgroup sl's x'' replaces its raw bytes, octet o stored at
-// 16 * (o ^ (sl & 7)) (eight consecutive subgroups then read the same octet
-// from eight different bank groups), and its (sx, f1, f2, 0) goes to
-// xm + 16 * sl. The eight lanes of a subgroup read their raw bytes before the
-// shuffles of stage_eight and write only inside that subgroup, so no lane
-// overwrites bytes another lane has yet to read.
+// Stages x (one vector) for the ring kernel: the raw bf16 x of subgroups
+// [sub_lo, sub_lo + nsub) lies densely at xr (128 bytes a subgroup, landed by
+// one bulk copy); subgroup sl gets a kXsB16-byte cell at xc + kXsB16 * sl, its
+// x'' with octet o (processing order) at 16 * o, then its (sx, f1, f2, 0).
+// The 16 bytes past each 128 put the same octet of 32 consecutive cells on
+// different banks.
 template <int BITS>
-__device__ __forceinline__ void stage_x_ring(uint32_t xs, uint32_t xm, int sub_lo, int nsub, int tid, int nthreads)
+__device__ __forceinline__ void stage_x_cells(uint32_t xr, uint32_t xc, int sub_lo, int nsub, int tid, int nthreads)
 {
     const int all = nsub * 8;
     const int all_pad = (all + nthreads - 1) / nthreads * nthreads;
     for (int u = tid; u < all_pad; u += nthreads) {
         const bool live = u < all;  // uniform over each eight-lane group
         const int sl = live ? u >> 3 : 0, e8 = u & 7;
-        const uint32_t cell = xs + uint32_t(sl) * 128u;
         uint4 raw = make_uint4(0, 0, 0, 0);
-        if (live) raw = lds_v4_u32(cell + uint32_t(e8) * 16u);
+        if (live) raw = lds_v4_u32(xr + uint32_t(sl) * 128u + uint32_t(e8) * 16u);
         uint4 packed;
         float4 meta;
         stage_eight<BITS, true>(raw, packed, meta);
         if (live) {
-            sts_v4_u32(cell + uint32_t(octet_position<BITS>(sub_lo + sl, e8) ^ (sl & 7)) * 16u, packed);
-            if (e8 == 0) sts_v4_u32(xm + uint32_t(sl) * 16u, make_uint4(__float_as_uint(meta.x), __float_as_uint(meta.y),
-                                                                       __float_as_uint(meta.z), 0u));
+            const uint32_t cell = xc + uint32_t(sl) * uint32_t(kXsB16);
+            sts_v4_u32(cell + uint32_t(octet_position<BITS>(sub_lo + sl, e8)) * 16u, packed);
+            if (e8 == 0) sts_v4_u32(cell + 128u, make_uint4(__float_as_uint(meta.x), __float_as_uint(meta.y),
+                                                            __float_as_uint(meta.z), 0u));
         }
     }
 }
@@ -694,13 +675,13 @@ __device__ __forceinline__ void stage_x_ring(uint32_t xs, uint32_t xm, int sub_l
 // from `quads`, its x'' at xsub (swizzle sw) and (sx, f1, f2) at xmeta;
 // returns the chunk value of row
 // lane >> 3 (all lanes of that row's eight-lane group hold it).
-template <int BITS>
+template <int BITS, bool SWZ = true>
 __device__ __forceinline__ float chunk_v1(const uint4 (&quads)[kRows][BITS == 4 ? 2 : 1], uint32_t xsub, uint32_t sw,
                                           uint32_t xmeta, const float (&fs)[kRows], const float (&fb)[kRows], bool active,
                                           int lane)
 {
     float ae[kRows], ao[kRows];
-    subgroup_dot_v1<BITS>(quads, xsub, sw, ae, ao);
+    subgroup_dot_v1<BITS, SWZ>(quads, xsub, sw, ae, ao);
     const float4 meta = lds_f4(xmeta);
     float val[4];
 #pragma unroll
@@ -829,7 +810,7 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CU
     // and the box start alignment in elements (16 bytes)
     constexpr int sbE = sb_elem_bytes(SBP), sbA = 16 / sbE;
     const uint32_t ring = smem_u32(smem + L.ring);
-    const uint32_t xs = smem_u32(smem + L.xs), xm = smem_u32(smem + L.xm);
+    const uint32_t xr = smem_u32(smem + L.xr), xc = smem_u32(smem + L.xc);
     float *cvs = reinterpret_cast<float *>(smem + L.cv);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar);  // full[slots], empty[slots], x
     unsigned *s_next = reinterpret_cast<unsigned *>(smem + L.misc);
@@ -889,9 +870,9 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CU
         }
     };
 
-    // The ring protocol needs every slot served by one producer (slots a
-    // multiple of the producer count) and at most one consumer per slot.
-    if (C > p.slots || C < 1 || P < 1 || p.slots % P != 0) {
+    // The ring protocol needs every slot served by one producer and consumed
+    // by one consumer warp: slots a multiple of both counts.
+    if (C > p.slots || C < 1 || P < 1 || p.slots % P != 0 || p.slots % C != 0) {
         if (tid == 0) atomicOr(p.err, 2u);
         return;
     }
@@ -953,34 +934,30 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CU
         }
     } else {
         // --------------------------------------------------------- consumers
+        // Consumer warp c takes units c, c + C, ...; with the slot count a
+        // multiple of C, slot s is only ever consumed by warp s % C, in unit
+        // order, so a unit's data is announced by its slot's phase parity
+        // alone: the producer refills a slot only after its one consumer has
+        // released the unit before.
         grid_dependency_wait();  // x may be written by the preceding grid
         if (tid == 0) {
-            // the CTA's x range in one copy, landing where it is staged
+            // the CTA's x range in one copy, landing where it is staged from
             mbar_arrive_expect_tx(xbar, uint32_t(nsub) * 128u);
-            bulk_load_plain(xs, p.x + size_t(sub_lo) * kSub, uint32_t(nsub) * 128u, xbar);
+            bulk_load_plain(xr, p.x + size_t(sub_lo) * kSub, uint32_t(nsub) * 128u, xbar);
         }
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(xbar, 0)) && lane == 0) {
             atomicOr(p.err, 1u);
             *s_abort = 1;
         }
-        stage_x_ring<BITS>(xs, xm, sub_lo, nsub, tid, C * 32);
+        stage_x_cells<BITS>(xr, xc, sub_lo, nsub, tid, C * 32);
         asm volatile("bar.sync 1, %0;" ::"r"(C * 32) : "memory");  // consumer warps only
 
         uint32_t poff[NP];
         piece_offsets<BITS>(lane, poff);
-        for (;;) {
-            int u = 0;
-            if (lane == 0) u = int(atomicAdd(s_next, 1u));
-            u = __shfl_sync(0xffffffffu, u, 0);
-            if (u >= nunits) break;
-            const int slot = u % p.slots;
-            // Wait by phase parity only once unit u is issued: issuing it
-            // required the slot's previous unit to be consumed, so the slot's
-            // barrier is then in the phase of unit u or just past it (data
-            // may arrive out of order, so grabbing alone does not ensure that).
+        int slot = warp, lap = 0;
+        for (int u = warp; u < nunits; u += C) {
             bool ok = !*s_abort;
-            if (ok) ok = wait_issued(s_issued + u % P, u);
-            if (ok) ok = mbar_wait_bounded(full0 + 8 * slot, (u / p.slots) & 1);
+            if (ok) ok = mbar_wait_bounded(full0 + 8 * slot, lap & 1);
             if (!__all_sync(0xffffffffu, ok)) {
                 if (lane == 0) {
                     atomicOr(p.err, 1u);
@@ -1008,7 +985,8 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CU
                 for (int r = 0; r < kRows; ++r) {
                     const int rr = r < g.nr ? r : 0;
                     const int bx = p.sb_mode_unit ? 0 : rr;
-                    const int xst = int(((long long)(g.r0 + bx) * p.G + g0) & ~(long long)(sbA - 1));
+                    // N * G < 2^31: element indices fit 32 bits
+                    const int xst = ((g.r0 + bx) * p.G + g0) & ~(sbA - 1);
                     sa[r] = base + L.sb_off + bx * L.sbs + sbE * ((g.r0 + rr) * p.G - xst);
                     ba[r] = sa[r] + nbox * L.sbs;
                 }
@@ -1039,13 +1017,18 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CU
                         fb[r] = bf16_bits_to_f32(lds_u16(ba[r] + go));
                     }
                 }
-                const uint32_t sl = uint32_t(tl - sub_lo);
-                const float tot = chunk_v1<BITS>(quads, xs + sl * 128u, sl & 7u, xm + sl * 16u, fs, fb, active, lane);
+                const uint32_t cell = xc + uint32_t(tl - sub_lo) * uint32_t(kXsB16);
+                const float tot = chunk_v1<BITS, false>(quads, cell, 0u, cell + 128u, fs, fb, active, lane);
                 const int r = lane >> 3;
                 if ((lane & 7) == 0 && r < g.nr) cvs[(g.r0 - row_t0 + r) * cpc_here + (cc - c_lo)] = tot;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+            slot += C;
+            if (slot >= p.slots) {
+                slot -= p.slots;
+                ++lap;
+            }
         }
     }
     __syncthreads();
@@ -1063,6 +1046,207 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CU
     }
     fold_chunks<1>(cvs, (rb_hi - rb_lo) * kRows, row_t0, c_lo, cpc_here, rb_lo, tid, nthreads, p.N, p.ks, p.cpc,
                    p.partials, p.counters, p.y, p.f32_out);
+}
+
+// ------------------------------------------------ one vector: direct loads --
+
+// Stages x (one vector) for qmv_one from global memory: subgroup sl of the
+// CTA's range [sub_lo, sub_lo + nsub) gets a kXsB16-byte cell at
+// xs + kXsB16 * sl: its x'' with octet o (processing order) at 16 * o, then
+// its (sx, f1, f2, 0). The 16 bytes past each 128 put the same octet of 32
+// consecutive cells on different banks.
+template <int BITS>
+__device__ __forceinline__ void stage_x_one(const uint16_t *x, uint32_t xs, int sub_lo, int nsub, int tid, int nthreads)
+{
+    const int all = nsub * 8;
+    const int all_pad = (all + nthreads - 1) / nthreads * nthreads;
+    for (int u = tid; u < all_pad; u += nthreads) {
+        const bool live = u < all;  // uniform over each eight-lane group
+        const int sl = live ? u >> 3 : 0, e8 = u & 7;
+        uint4 raw = make_uint4(0, 0, 0, 0);
+        if (live) raw = __ldg(reinterpret_cast<const uint4 *>(x + size_t(sub_lo + sl) * kSub) + e8);
+        uint4 packed;
+        float4 meta;
+        stage_eight<BITS, true>(raw, packed, meta);
+        if (live) {
+            const uint32_t cell = xs + uint32_t(sl) * uint32_t(kXsB16);
+            sts_v4_u32(cell + uint32_t(octet_position<BITS>(sub_lo + sl, e8)) * 16u, packed);
+            if (e8 == 0) sts_v4_u32(cell + 128u, make_uint4(__float_as_uint(meta.x), __float_as_uint(meta.y),
+                                                            __float_as_uint(meta.z), 0u));
+        }
+    }
+}
+
+// The one-vector kernel. CTA (i, j) owns row blocks [rb_lo, rb_hi) and chunks
+// [c_lo, c_hi); its units are the (row block, chunk) pairs in row-block-major
+// order. Warp w computes units w, w + W, ... (W warps): it loads a unit's
+// weights (the lane's subgroup of 4 rows, two or one 16-byte loads per row),
+// scales and biases straight into registers, and issues the next unit's loads
+// before computing the current one. The first unit's loads go out before the
+// wait for the preceding grid: weights, scales and biases never depend on it.
+// Unit bookkeeping is incremental (no division per unit): the kernel issues
+// about 1.7 instructions per weight in its datapath, which is what bounds it.
+template <int BITS, int GS, bool SBP>
+__device__ __forceinline__ void qmv_one_body(const Params &p)
+{
+    constexpr int kSubB = sub_bytes(BITS);
+    constexpr int NP = BITS == 4 ? 2 : 1;
+
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+
+    const int c_lo = blockIdx.y * p.cpc;
+    const int c_hi = c_lo + p.cpc < p.ks ? c_lo + p.cpc : p.ks;
+    const int sub_lo = c_lo * kChunkSubs;
+    const int sub_hi = c_hi * kChunkSubs < p.S_row ? c_hi * kChunkSubs : p.S_row;
+    const int nsub = sub_hi - sub_lo;
+    const int rb_lo = int((long long)blockIdx.x * p.NB / p.grid_rows);
+    const int rb_hi = int((long long)(blockIdx.x + 1) * p.NB / p.grid_rows);
+    const int nrb = rb_hi - rb_lo;
+    const int row_t0 = rb_lo * kRows;
+    const int cpc_here = c_hi - c_lo;
+
+    const int nsub_max = p.cpc * kChunkSubs < p.S_row ? p.cpc * kChunkSubs : p.S_row;
+    const OneLayout L = one_layout(nsub_max, p.max_rb, p.cpc);
+    const uint32_t xs = smem_u32(smem + L.xs);
+    float *cvs = reinterpret_cast<float *>(smem + L.cv);
+
+    // Unit stepping: (rbl, ccl) = unit u of the CTA, advanced by W units at a
+    // time (dr row blocks and dc chunks, one more row block on a carry). The
+    // lane's byte offset of a unit's row 0 piece and the element index of its
+    // row 0 metadata advance by fixed deltas, so no unit needs a multiply.
+    const int dr = nwarps / cpc_here, dc = nwarps - dr * cpc_here;
+    const long long rbB = (long long)kRows * p.row_bytes;  // bytes of one row block
+    const long long wstep0 = dr * rbB + (long long)dc * chunk_bytes(BITS);
+    const long long wstep1 = wstep0 + rbB - (long long)cpc_here * chunk_bytes(BITS);
+    const int rbG = kRows * p.G;  // metadata elements of one row block (N * G < 2^31)
+    constexpr int kGpc = kChunkElems / GS;  // groups per chunk
+    const int estep0 = dr * rbG + dc * kGpc, estep1 = estep0 + rbG - cpc_here * kGpc;
+    // Per lane: the offset of its first piece inside a subgroup row (4-bit:
+    // the half selected by bit 2 of the lane, i.e. of the subgroup index,
+    // first) and of the second; the last subgroup of a row for clamping.
+    const int first = BITS == 4 ? ((lane >> 2) & 1) * 16 : 0;
+    const int second = 16 - first;
+    const int t_last = p.S_row - 1;
+    const int sub_off = lane * kSubB;  // the lane's subgroup inside a chunk row
+
+    int rbl = warp / cpc_here, ccl = warp - (warp / cpc_here) * cpc_here;
+    // byte offset of the unit's chunk row 0 and element index of its row 0
+    // metadata, without the lane's subgroup
+    long long wo = (long long)(rb_lo + rbl) * rbB + (long long)(c_lo + ccl) * chunk_bytes(BITS);
+    int eo = (rb_lo + rbl) * rbG + (c_lo + ccl) * kGpc;
+
+    // Loads of the unit at (wo, eo), chunk ccl, row block rbl. Rows past N
+    // re-read row 0 of the block and subgroups past the row's end re-read the
+    // row's last subgroup (their results are discarded).
+    auto load_unit = [&](long long wo_u, int eo_u, int rbl_u, int ccl_u, uint4 (&wq)[kRows][NP], uint32_t (&sv)[kRows],
+                         uint32_t (&bv)[kRows]) {
+        const int t = (c_lo + ccl_u) * kChunkSubs + lane;
+        const int clamp = t > t_last ? t - t_last : 0;  // subgroups to step back
+        const int nr = p.N - (rb_lo + rbl_u) * kRows;
+        const uint8_t *w0 = p.w + wo_u + (sub_off - clamp * kSubB);
+        const int e0 = eo_u + ((lane - clamp) * (kSub / 32)) / (GS / 32);
+        if (nr >= kRows) {
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) {
+                const uint8_t *wr = w0 + r * (long long)p.row_bytes;
+                wq[r][0] = __ldcs(reinterpret_cast<const uint4 *>(wr + first));
+                if constexpr (NP == 2) wq[r][1] = __ldcs(reinterpret_cast<const uint4 *>(wr + second));
+                const int e = e0 + r * p.G;
+                if constexpr (SBP) {  // one pair: scale in the low half, bias in the high half
+                    const uint32_t v = __ldcs(reinterpret_cast<const unsigned int *>(p.scales) + e);
+                    sv[r] = v & 0xFFFFu;
+                    bv[r] = v >> 16;
+                } else {
+                    sv[r] = __ldcs(reinterpret_cast<const unsigned short *>(p.scales) + e);
+                    bv[r] = __ldcs(reinterpret_cast<const unsigned short *>(p.biases) + e);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) {
+                const int ro = r < nr ? r : 0;
+                const uint8_t *wr = w0 + ro * (long long)p.row_bytes;
+                wq[r][0] = __ldcs(reinterpret_cast<const uint4 *>(wr + first));
+                if constexpr (NP == 2) wq[r][1] = __ldcs(reinterpret_cast<const uint4 *>(wr + second));
+                const int e = e0 + ro * p.G;
+                if constexpr (SBP) {
+                    const uint32_t v = __ldcs(reinterpret_cast<const unsigned int *>(p.scales) + e);
+                    sv[r] = v & 0xFFFFu;
+                    bv[r] = v >> 16;
+                } else {
+                    sv[r] = __ldcs(reinterpret_cast<const unsigned short *>(p.scales) + e);
+                    bv[r] = __ldcs(reinterpret_cast<const unsigned short *>(p.biases) + e);
+                }
+            }
+        }
+    };
+    // Steps 1-3 of unit (rbl_u, ccl_u) from its registers; its chunk value of
+    // row lane >> 3 goes to shared memory.
+    auto compute_unit = [&](int rbl_u, int ccl_u, const uint4 (&wq)[kRows][NP], const uint32_t (&sv)[kRows],
+                            const uint32_t (&bv)[kRows]) {
+        const int t = (c_lo + ccl_u) * kChunkSubs + lane;
+        const bool active = t <= t_last;
+        const uint32_t sl = uint32_t((active ? t : t_last) - sub_lo);
+        float fs[kRows], fb[kRows];
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+            fs[r] = bf16_bits_to_f32(sv[r]);
+            fb[r] = bf16_bits_to_f32(bv[r]);
+        }
+        const uint32_t cell = xs + sl * uint32_t(kXsB16);
+        const float tot = chunk_v1<BITS, false>(wq, cell, 0u, cell + 128u, fs, fb, active, lane);
+        const int r = lane >> 3;
+        if ((lane & 7) == 0 && r < p.N - (rb_lo + rbl_u) * kRows) cvs[(rbl_u * kRows + r) * cpc_here + ccl_u] = tot;
+    };
+    auto advance = [&](int &rb_u, int &cc_u, long long &wo_u, int &eo_u) {
+        cc_u += dc;
+        rb_u += dr;
+        const bool carry = cc_u >= cpc_here;
+        if (carry) {
+            cc_u -= cpc_here;
+            ++rb_u;
+        }
+        wo_u += carry ? wstep1 : wstep0;
+        eo_u += carry ? estep1 : estep0;
+    };
+
+
+    // Two register sets, A and B, alternate: while one unit is computed the
+    // next one's loads are in flight.
+    uint4 wa[kRows][NP], wb[kRows][NP];
+    uint32_t sa[kRows] = {0, 0, 0, 0}, ba[kRows] = {0, 0, 0, 0}, sb[kRows] = {0, 0, 0, 0}, bb[kRows] = {0, 0, 0, 0};
+    if (rbl < nrb) load_unit(wo, eo, rbl, ccl, wa, sa, ba);
+    grid_launch_dependents();
+    grid_dependency_wait();  // x may be written by the preceding grid
+    stage_x_one<BITS>(p.x, xs, sub_lo, nsub, tid, nthreads);
+    __syncthreads();
+
+    while (rbl < nrb) {
+        int rb1 = rbl, cc1 = ccl, eo1 = eo;
+        long long wo1 = wo;
+        advance(rb1, cc1, wo1, eo1);
+        if (rb1 < nrb) load_unit(wo1, eo1, rb1, cc1, wb, sb, bb);
+        compute_unit(rbl, ccl, wa, sa, ba);
+        if (rb1 >= nrb) break;
+        rbl = rb1;
+        ccl = cc1;
+        wo = wo1;
+        eo = eo1;
+        advance(rb1, cc1, wo1, eo1);
+        if (rb1 < nrb) load_unit(wo1, eo1, rb1, cc1, wa, sa, ba);
+        compute_unit(rbl, ccl, wb, sb, bb);
+        rbl = rb1;
+        ccl = cc1;
+        wo = wo1;
+        eo = eo1;
+    }
+    __syncthreads();
+    fold_chunks<1>(cvs, nrb * kRows, row_t0, c_lo, cpc_here, rb_lo, tid, nthreads, p.N, p.ks, p.cpc, p.partials,
+                   p.counters, p.y, p.f32_out);
 }
 
 // ------------------------------------------------ V vectors: direct loads --
@@ -1250,6 +1434,15 @@ __global__ void __launch_bounds__(kThreadsV1, 1)
            const __grid_constant__ CUtensorMap map_b, const RingParams p)
 {
     qmv_ring_body<BITS, GS, SBP>(&map_w, &map_s, &map_b, p);
+}
+
+// The one-vector kernel: kOneWarps warps, kOneCtasPerSm CTAs per SM.
+constexpr int kOneWarps = 12;
+constexpr int kOneCtasPerSm = 1;
+template <int BITS, int GS, bool SBP>
+__global__ void __launch_bounds__(kOneWarps * 32, kOneCtasPerSm) qmv_one(const Params p)
+{
+    qmv_one_body<BITS, GS, SBP>(p);
 }
 
 template <int BITS, int GS, int V, bool SBP>

@@ -13,6 +13,7 @@ namespace qmv {
 
 static_assert(kConsumersV1 == kRingConsumers && kProducersV1 == kRingProducers, "launch bounds");
 static_assert(kThreadsVN == kStreamedWarps * 32, "launch bounds");
+static_assert(kOneWarps == kOneWarpsDecl && kOneCtasPerSm == kOneCtasPerSmDecl, "launch bounds");
 
 template <typename Kern, typename... Args>
 cudaError_t launch_one(Kern kern, std::atomic<int> (&configured)[64], const Launch &l, cudaStream_t stream, Args... args)
@@ -55,6 +56,14 @@ cudaError_t launch_m1(const RingMaps &maps, const RingParams &p, const Launch &l
     static std::atomic<int> configured[2][64] = {};
     if (p.sb_packed) return launch_one(qmv_m1<BITS, GS, true>, configured[1], l, stream, maps.w, maps.s, maps.b, p);
     return launch_one(qmv_m1<BITS, GS, false>, configured[0], l, stream, maps.w, maps.s, maps.b, p);
+}
+
+template <int BITS, int GS>
+cudaError_t launch_one_vector(const Params &p, const Launch &l, cudaStream_t stream)
+{
+    static std::atomic<int> configured[2][64] = {};
+    if (p.sb_packed) return launch_one(qmv_one<BITS, GS, true>, configured[1], l, stream, p);
+    return launch_one(qmv_one<BITS, GS, false>, configured[0], l, stream, p);
 }
 
 template <int BITS, int GS, int V>

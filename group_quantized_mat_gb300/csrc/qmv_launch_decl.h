@@ -14,6 +14,9 @@ namespace qmv {
 constexpr int kStreamedWarps = 12;
 constexpr int kRingConsumers = 16;
 constexpr int kRingProducers = 4;
+// The one-vector kernel qmv_one: warps per CTA and CTAs per SM.
+constexpr int kOneWarpsDecl = 12;
+constexpr int kOneCtasPerSmDecl = 1;
 
 // Tensor maps of the one-vector kernel: weights (tiles only), scales, biases.
 struct RingMaps {
@@ -49,6 +52,7 @@ cudaError_t launch_mxfp4(int V, const MxParams &p, cudaStream_t stream);
 
 #define QMV_DECLARE_LAUNCH(name)                                                                                  \
     cudaError_t name##_m1(const RingMaps &maps, const RingParams &p, const Launch &l, cudaStream_t stream);      \
+    cudaError_t name##_one(const Params &p, const Launch &l, cudaStream_t stream);                               \
     cudaError_t name##_streamed(int V, const Params &p, const Launch &l, cudaStream_t stream);                   \
     cudaError_t name##_stage(const uint16_t *x, int K, int S_row, int V, uint8_t *out, unsigned *counters,       \
                              int ncounters, bool pdl, cudaStream_t stream);

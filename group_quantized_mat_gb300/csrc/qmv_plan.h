@@ -95,14 +95,30 @@ __host__ __device__ inline SmemLayout smem_layout(int bits, int V, int warps, in
     return L;
 }
 
-// Shared memory of the one-vector kernel, as byte offsets from a 128-aligned
-// base: the ring, staged x'' (128 bytes a subgroup, where the raw x lands
-// first) and its (sx, f1, f2, 0), chunk values, the slot barriers and the x
-// barrier, counters.
+// Shared memory of the one-vector kernel qmv_one, as byte offsets from a
+// 128-aligned base: staged x'' cells (kXsB16 bytes a subgroup: 128 bytes of
+// x'' and its (sx, f1, f2, 0)), chunk values.
+struct OneLayout {
+    int xs, cv, total;
+};
+
+__host__ __device__ inline OneLayout one_layout(int nsub, int max_rb, int cpc)
+{
+    OneLayout L;
+    L.xs = 0;
+    L.cv = align_up(nsub * kXsB16, 16);
+    L.total = L.cv + max_rb * kRows * cpc * 4 + 128;  // slack for aligning the dynamic base
+    return L;
+}
+
+// Shared memory of the one-vector ring kernel, as byte offsets from a
+// 128-aligned base: the ring, the raw x (128 bytes a subgroup, landed by one
+// bulk copy), the staged x'' cells (kXsB16 bytes a subgroup), chunk values,
+// the slot barriers and the x barrier, counters.
 constexpr int kBoxAlign = 128;  // shared-memory alignment of a tensor-map box
 struct RingLayout {
     int slot_bytes, sb_off, sbs;  // slot size, offset of the scale/bias boxes in a slot, bytes per box
-    int ring, xs, xm, cv, bar, misc, total;
+    int ring, xr, xc, cv, bar, misc, total;
 };
 
 // Metadata element bytes: a bf16 scale or bias, or an interleaved pair.
@@ -117,9 +133,9 @@ __host__ __device__ inline RingLayout ring_layout(int pitch, int sb_mode_unit, i
     // boxes per slot: one per unit or one per row, of each metadata tensor
     L.slot_bytes = L.sb_off + (sb_mode_unit ? 1 : kRows) * (sb_packed ? 1 : 2) * L.sbs;
     L.ring = 0;
-    L.xs = slots * L.slot_bytes;
-    L.xm = L.xs + nsub * 128;
-    L.cv = align_up(L.xm + nsub * 16, 16);
+    L.xr = slots * L.slot_bytes;
+    L.xc = L.xr + nsub * 128;
+    L.cv = align_up(L.xc + nsub * kXsB16, 16);
     L.bar = align_up(L.cv + max_rb * kRows * cpc * 4, 16);
     L.misc = L.bar + (2 * slots + 1) * 8;
     L.total = L.misc + 32 + kBoxAlign;  // next-unit counter, abort flag, issued counts; alignment slack
