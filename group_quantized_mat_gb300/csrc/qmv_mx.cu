@@ -29,13 +29,16 @@
 // f16 -> f32 widening each; the two chains run as one packed fma.rn.f32x2.
 //
 // A CTA holds 8 warps of 4 rows each. K goes by in chunks of 1024 elements,
-// one 32-block per lane; each chunk of x (all V vectors) is staged once per
-// CTA into shared memory as fp32 pairs laid out [vector][pair][lane], so that
-// a warp's read of one pair per lane is 256 contiguous bytes. With several
-// vectors the next chunk's weight vectors and scale bytes are loaded while the
-// current one is computed. A chunk's weights convert once per pass of up to 4
-// vectors, and
-// every x pair read from shared memory serves the warp's 4 rows.
+// one 32-block per lane; each chunk of x is staged once per CTA into shared
+// memory as fp32 pairs laid out [vector][pair][lane], so that a warp's read of
+// one pair per lane is 256 contiguous bytes, and every x pair read serves the
+// warp's 4 rows. Up to 4 vectors: all of them are staged per chunk, a chunk's
+// weights convert once per pass of up to 4 vectors, and (2..4 vectors) the
+// next chunk's weights are loaded while the current one is computed. From 5
+// vectors on, the vectors go in passes of at most 5 outermost, each over all
+// of K with its partials in registers (mx_pass), so a chunk's weights convert
+// once per pass and a CTA needs at most 20 KB of shared memory: two CTAs (16
+// warps) share an SM.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -126,12 +129,144 @@ __device__ __forceinline__ void mx_stage_chunk(uint64_t *xs, const uint16_t *x, 
 
 // CTAs per SM the register budget must allow: four for one vector (at most
 // 64 registers), so that a 15360-row matrix (480 CTAs) runs as one wave on
-// 152 SMs; two for 2..4 vectors.
+// 152 SMs; two otherwise (at most 128 registers).
 template <int V>
-constexpr int mx_min_blocks() { return V == 1 ? 4 : V <= 4 ? 2 : 1; }
+constexpr int mx_min_blocks() { return V == 1 ? 4 : 2; }
+
+// Several vectors (V >= 5): the vectors go in passes of at most kMxWidePass,
+// each pass running over all of K, so that a pass's partials stay in
+// registers and the chunk's x is staged for the pass's vectors only. Each
+// pass re-reads the warp's weights, which the first pass has just brought
+// into L2. Vectors [v0, v0 + VPN) of the warp's rows, steps 1-4.
+constexpr int kMxWidePass = 5;
+
+template <int VPN>
+__device__ __forceinline__ void mx_pass(const MxParams &p, uint64_t *xs, int v0, int row0, int nlive, int lane)
+{
+    const int B = p.K >> 5;
+    const int nchunks = (B + 31) >> 5;
+    const uint4 *wbase = reinterpret_cast<const uint4 *>(p.w) + size_t(row0) * B;
+    const uint8_t *sbase = p.scales + size_t(row0) * B;
+    const uint16_t *xv = p.x + size_t(v0) * p.K;
+
+    float part[VPN][kMxRows];
+#pragma unroll
+    for (int v = 0; v < VPN; ++v)
+#pragma unroll
+        for (int r = 0; r < kMxRows; ++r) part[v][r] = 0.0f;
+
+#pragma unroll 1
+    for (int c = 0; c < nchunks; ++c) {
+        const int k0 = c * kMxChunk;
+        const int kn = p.K - k0 < kMxChunk ? p.K - k0 : kMxChunk;
+        const int b = c * 32 + lane;
+        uint4 wc[kMxRows];
+        uint32_t sc[kMxRows];
+#pragma unroll
+        for (int r = 0; r < kMxRows; ++r) {
+            const bool ok = r < nlive && b < B;
+            wc[r] = ok ? __ldg(wbase + size_t(r) * B + b) : make_uint4(0u, 0u, 0u, 0u);
+            sc[r] = ok ? __ldg(sbase + size_t(r) * B + b) : 0u;
+        }
+        __syncthreads();  // every warp is done reading the previous chunk of x
+        mx_stage_chunk<VPN>(xs, xv, p.K, k0, kn);
+        __syncthreads();
+        if (b < B) {
+            uint64_t acc[VPN][kMxRows];
+#pragma unroll
+            for (int v = 0; v < VPN; ++v)
+#pragma unroll
+                for (int r = 0; r < kMxRows; ++r) acc[v][r] = 0ull;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t h[kMxRows][4];
+#pragma unroll
+                for (int r = 0; r < kMxRows; ++r) {
+                    const uint32_t word = j == 0 ? wc[r].x : j == 1 ? wc[r].y : j == 2 ? wc[r].z : wc[r].w;
+                    e2m1x8_to_f16x2(word, h[r]);
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int i = 4 * j + k;
+                    uint64_t wv[kMxRows];
+#pragma unroll
+                    for (int r = 0; r < kMxRows; ++r) wv[r] = f16x2_to_f32x2(h[r][k]);
+#pragma unroll
+                    for (int v = 0; v < VPN; ++v) {
+                        const uint64_t x2 = xs[(v * kMxPairs + i) * 32 + lane];
+#pragma unroll
+                        for (int r = 0; r < kMxRows; ++r) acc[v][r] = mx_ffma2(wv[r], x2, acc[v][r]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < kMxRows; ++r) {
+                const float scale = e8m0_to_f32(sc[r]);
+#pragma unroll
+                for (int v = 0; v < VPN; ++v) {
+                    const float ae = __uint_as_float(uint32_t(acc[v][r]));
+                    const float ao = __uint_as_float(uint32_t(acc[v][r] >> 32));
+                    part[v][r] = __fadd_rn(part[v][r], __fmul_rn(__fadd_rn(ae, ao), scale));
+                }
+            }
+        }
+    }
+    // butterfly over the lanes: every lane ends with the same sum
+#pragma unroll
+    for (int v = 0; v < VPN; ++v)
+#pragma unroll
+        for (int r = 0; r < kMxRows; ++r) {
+            float sum = part[v][r];
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, off));
+            part[v][r] = sum;
+        }
+#pragma unroll
+    for (int r = 0; r < kMxRows; ++r) {
+        if (lane != r || r >= nlive) continue;
+        const size_t n = size_t(row0 + r);
+#pragma unroll
+        for (int v = 0; v < VPN; ++v) {
+            if (p.f32_out)
+                static_cast<float *>(p.y)[size_t(v0 + v) * p.N + n] = part[v][r];
+            else
+                static_cast<__nv_bfloat16 *>(p.y)[size_t(v0 + v) * p.N + n] = __float2bfloat16_rn(part[v][r]);
+        }
+    }
+}
+
+// Pass structure of a V-vector launch with V >= 5: passes of VP vectors, the
+// last one of the remainder.
+template <int V>
+struct MxPasses {
+    static constexpr int N = (V + kMxWidePass - 1) / kMxWidePass;
+    static constexpr int VP = (V + N - 1) / N;
+    static constexpr int LAST = V - (N - 1) * VP;
+};
+
+template <int V>
+__device__ __forceinline__ void qmv_mxfp4_narrow(MxParams p);
 
 template <int V>
 __global__ void __launch_bounds__(kMxWarps * 32, mx_min_blocks<V>()) qmv_mxfp4(MxParams p)
+{
+    if constexpr (V >= 5) {
+        extern __shared__ __align__(16) uint64_t mx_xs[];  // [VP][kMxPairs][32] fp32 pairs
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        const int row0 = blockIdx.x * kMxRowsPerCta + warp * kMxRows;
+        const int nlive = p.N - row0;
+        using PS = MxPasses<V>;
+#pragma unroll 1
+        for (int ps = 0; ps + 1 < PS::N; ++ps) mx_pass<PS::VP>(p, mx_xs, ps * PS::VP, row0, nlive, lane);
+        mx_pass<PS::LAST>(p, mx_xs, (PS::N - 1) * PS::VP, row0, nlive, lane);
+        return;
+    } else {
+        qmv_mxfp4_narrow<V>(p);
+    }
+}
+
+template <int V>
+__device__ __forceinline__ void qmv_mxfp4_narrow(MxParams p)
 {
     extern __shared__ __align__(16) uint64_t mx_xs[];  // [V][kMxPairs][32] fp32 pairs
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -266,7 +401,9 @@ cudaError_t launch_mx_v(const MxParams &p, cudaStream_t stream)
     // The opt-in dynamic shared-memory limit is a per-device kernel attribute;
     // raise it (never lower it) under a lock the first time a device needs it.
     static std::atomic<int> configured[64] = {};
-    const int smem = V * kMxPairs * 32 * int(sizeof(uint64_t));
+    // staged x: the launch's vectors, or (V >= 5) one pass's
+    constexpr int VS = V >= 5 ? MxPasses<V >= 5 ? V : 5>::VP : V;
+    const int smem = VS * kMxPairs * 32 * int(sizeof(uint64_t));
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
