@@ -85,6 +85,16 @@ constexpr int kMaxSlots = 32;
 constexpr int kRingMinK = 12288;
 
 
+// The widest chunk range that fits (cpc_max) split into equal ranges: as many
+// ranges as cpc_max needs, each ceil(ks / ranges) chunks, so that no CTA
+// carries a much longer range than another.
+int balanced_cpc(int ks, int cpc_max)
+{
+    if (cpc_max < 1) cpc_max = 1;
+    const int nranges = (ks + cpc_max - 1) / cpc_max;
+    return (ks + nranges - 1) / nranges;
+}
+
 void common_shape(Problem &pr, int V, int N, int K, int bits, int gs)
 {
     pr.V = V; pr.N = N; pr.K = K; pr.bits = bits; pr.gs = gs;
@@ -125,6 +135,7 @@ Problem plan_direct(int V, int N, int K, int bits, int gs, int sms)
     auto xs_bytes = [&](int cpc) { return qmv::align_up(V * nsub_of(cpc) * qmv::kXsF32, 16); };
     pr.cpc = pr.ks;
     while (pr.cpc > 1 && xs_bytes(pr.cpc) + kCvBudget + wbuf + 16 + 128 > kSmemBudget) --pr.cpc;
+    pr.cpc = balanced_cpc(pr.ks, pr.cpc);
     pr.threads = 32 * warps;
     // chunk values may use whatever shared memory the x cells and the weight
     // buffer leave (at least kCvBudget, by the fit above)
@@ -145,7 +156,7 @@ Problem plan_ring(int N, int K, int bits, int gs, int sms, bool sb_packed)
     common_shape(pr, 1, N, K, bits, gs);
     // raw x (128 bytes a subgroup) and its staged cell (kXsB16 bytes)
     const int per_sub = 128 + qmv::kXsB16;
-    pr.cpc = pr.S_row * per_sub <= kXsBudgetV1 ? pr.ks : kXsBudgetV1 / (qmv::kChunkSubs * per_sub);
+    pr.cpc = pr.S_row * per_sub <= kXsBudgetV1 ? pr.ks : balanced_cpc(pr.ks, kXsBudgetV1 / (qmv::kChunkSubs * per_sub));
     pr.consumers = qmv::kRingConsumers;
     grid_shape(pr, sms, 1, kCvBudget);
     const int cb = qmv::chunk_bytes(bits);
@@ -211,7 +222,7 @@ Problem plan_one(int N, int K, int bits, int gs, int sms, bool sb_packed)
     Problem pr{};
     common_shape(pr, 1, N, K, bits, gs);
     const int per_chunk = qmv::kChunkSubs * qmv::kXsB16;
-    pr.cpc = pr.S_row * qmv::kXsB16 <= kXsBudgetOne ? pr.ks : kXsBudgetOne / per_chunk;
+    pr.cpc = pr.S_row * qmv::kXsB16 <= kXsBudgetOne ? pr.ks : balanced_cpc(pr.ks, kXsBudgetOne / per_chunk);
     grid_shape(pr, sms * qmv::kOneCtasPerSmDecl, 1, kCvBudgetOne);
     pr.threads = 32 * qmv::kOneWarpsDecl;
     const int nsub = pr.cpc * qmv::kChunkSubs < pr.S_row ? pr.cpc * qmv::kChunkSubs : pr.S_row;
