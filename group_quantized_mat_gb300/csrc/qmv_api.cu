@@ -196,11 +196,22 @@ Problem plan_ring(int N, int K, int bits, int gs, int sms, bool sb_packed)
         return qmv::ring_layout(pr.pitch, pr.sb_mode_unit, pr.sbox, pr.sb_packed, slots, nsub, pr.max_rb, pr.cpc);
     };
     // Slots: a multiple of the producer and the consumer counts (each slot
-    // has one producer and one consumer warp); fewer consumer warps when the
-    // ring of one slot per consumer does not fit.
+    // has one producer and one consumer warp). A consumer warp with a single
+    // slot waits a full memory latency between its units, so the largest
+    // consumer count whose ring gives every consumer two slots is taken;
+    // failing that, one slot per consumer (fewer consumers if even that does
+    // not fit).
     const int P = qmv::kRingProducers;
-    int C = qmv::kRingConsumers;
-    while (C > P && layout(C).total > kSmemBudget) C /= 2;
+    int C = 0;
+    for (int c : {qmv::kRingConsumers, 12, 8})
+        if (c <= qmv::kRingConsumers && layout(2 * c).total <= kSmemBudget) {
+            C = c;
+            break;
+        }
+    if (C == 0) {
+        C = qmv::kRingConsumers;
+        while (C > P && layout(C).total > kSmemBudget) C /= 2;
+    }
     int slots = C;
     while (slots + C <= kMaxSlots && layout(slots + C).total <= kSmemBudget) slots += C;
     pr.consumers = C;
