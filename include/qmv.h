@@ -137,7 +137,8 @@ QMV_API size_t qmv_workspace_size(int M, int N, int K, int bits, int group_size)
  * once to bf16 (nearest even). The fp32 operation order for an output element
  * depends only on (N, K, bits, group_size) and the element's row: column j of
  * an M-vector call is bit-identical to an M = 1 call on x[j] (issue #1289
- * "The observation this rests on": "bit-identical ... by construction").
+ * "The observation this rests on": identity that follows from the arithmetic
+ * itself, not from a tolerance).
  *
  * The call returns after enqueueing. Most calls need no scratch (M = 1 with
  * the whole of K per CTA); M >= 2, and problems whose CTAs split K, need a
