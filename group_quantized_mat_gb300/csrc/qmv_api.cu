@@ -416,6 +416,13 @@ cudaError_t dispatch(const Problem &pr, const qmv::RingMaps &maps, const qmv::Pa
         cudaError_t e = cudaMemsetAsync(p.counters, 0, counter_bytes(pr.NB), stream);
         if (e != cudaSuccess) return e;
     }
+    if (pr.V == 1 && !p.counters) {
+        // A one-vector launch always carries a programmatic dependency: its
+        // set-up (barriers, tensor maps, shared memory) overlaps the tail of
+        // the preceding kernel, and it reads nothing before waiting for that
+        // kernel unless QMV_PDL allows the weights to stream under it.
+        l.pdl = true;
+    }
     if (pr.V == 1 && pr.unit_mode == kUnitOne) {
         if (pr.bits == 4 && pr.gs == 64) return qmv::launch_b4g64_one(p, l, stream);
         if (pr.bits == 4 && pr.gs == 128) return qmv::launch_b4g128_one(p, l, stream);
@@ -542,6 +549,7 @@ qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t 
         p.NB = pr.NB; p.grid_rows = pr.grid_rows; p.cpc = pr.cpc; p.max_rb = pr.max_rb;
         p.f32_out = f32_out ? 1 : 0;
         p.sb_packed = sb_packed ? 1 : 0;
+        p.early_weights = pdl ? 1 : 0;
         const bool split = split_bytes(pr) > 0;
         p.counters = split ? static_cast<unsigned *>(workspace) : nullptr;
         p.partials = split ? reinterpret_cast<float *>(static_cast<char *>(workspace) + counter_bytes(pr.NB)) : nullptr;

@@ -892,8 +892,10 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CU
         // --------------------------------------------------------- producers
         // Producer k issues units k, k + P, ... (so it alone serves the slots
         // congruent to k modulo P), each after the slot's previous unit was
-        // consumed. Weight, scale and bias tiles do not depend on the
-        // preceding grid, so the producers never wait for it (nor for x).
+        // consumed. The launch may overlap the preceding grid: unless the
+        // caller allowed weights to be read under it, the producers wait for it
+        // before their first copy.
+        if (!p.early_weights) grid_dependency_wait();
         const int kp = warp - C;
         bool ok = true;
         int slot = kp, lap = 0, rbl = 0, pc = kp;
@@ -1219,6 +1221,7 @@ __device__ __forceinline__ void qmv_one_body(const Params &p)
     // next one's loads are in flight.
     uint4 wa[kRows][NP], wb[kRows][NP];
     uint32_t sa[kRows] = {0, 0, 0, 0}, ba[kRows] = {0, 0, 0, 0}, sb[kRows] = {0, 0, 0, 0}, bb[kRows] = {0, 0, 0, 0};
+    if (!p.early_weights) grid_dependency_wait();  // the launch may overlap the preceding grid
     if (rbl < nrb) load_unit(wo, eo, rbl, ccl, wa, sa, ba);
     grid_launch_dependents();
     grid_dependency_wait();  // x may be written by the preceding grid

@@ -52,6 +52,8 @@ struct Params {
     int f32_out;
     const uint8_t *xs_staged; // streamed kernel: the call's staged cells [V][S_row] (qmv_stage_x)
     int sb_packed;            // 1: scales is the interleaved uint32 array (scale low, bias high), biases unused
+    int early_weights;        // one-vector kernels: 1 = weights, scales, biases may be read before the wait for
+                              // the preceding grid (QMV_PDL); 0 = nothing is read before that wait
 };
 
 // The one-vector kernel's ring: units are (row block, piece) pairs, a piece

@@ -168,7 +168,10 @@ QMV_API qmv_status qmv_run(const uint32_t *w_q, const uint16_t *scales, const ui
  * the call may start streaming w_q, scales and biases before that kernel has
  * finished (x, y and the workspace are touched only after it has). Set it only
  * when the preceding kernel does not write w_q, scales or biases -- the
- * decode-loop case, where weights are constant. */
+ * decode-loop case, where weights are constant. (Without the flag a one-vector
+ * launch that needs no scratch still carries a programmatic dependency, so that
+ * its set-up overlaps the preceding kernel's tail, but it reads and writes
+ * nothing before that kernel has completed: stream order is unchanged.) */
 #define QMV_PDL 0x4u
 /* `scales` is the uint32 [N, K/group_size] array of qmv_pack_sb (16-byte
  * aligned); `biases` is not read and may be NULL. */
