@@ -30,8 +30,8 @@
 //
 // A CTA holds 8 warps of 4 rows each. K goes by in chunks of 1024 elements,
 // one 32-block per lane; each chunk of x is staged once per CTA into shared
-// memory as fp32 pairs laid out [vector][pair][lane], so that a warp's read of
-// one pair per lane is 256 contiguous bytes, and every x pair read serves the
+// memory as fp32 pairs laid out [vector][pair / 2][lane][pair % 2] (a warp's
+// reads of two pairs cover 512 contiguous bytes), and every x pair read serves the
 // warp's 4 rows. Up to 4 vectors: all of them are staged per chunk, a chunk's
 // weights convert once per pass of up to 4 vectors, and (2..4 vectors) the
 // next chunk's weights are loaded while the current one is computed. From 5
@@ -105,11 +105,19 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t e)
     return __uint_as_float(bits);
 }
 
-// Stages x[v][k0 .. k0 + kn) for v < V into xs[v][pair][lane] as fp32 pairs
-// (element 32 l + 2 i in the low half of xs[v][i][l]). kn is a multiple of 32.
-// Thread item t of a vector takes the 8 elements (t / 32) * 8 .. + 7 of block
-// t % 32, so the 32 threads of a warp write 32 consecutive lanes of one pair
-// row: every shared-memory store is conflict-free.
+// Staged x of a chunk: pair i (elements 32 l + 2 i, 32 l + 2 i + 1) of vector
+// v for lane l, laid out [v][i / 2][l][i % 2], so that a lane's pairs 2j and
+// 2j + 1 are one 16-byte vector and a warp's read of one pair is 16 bytes a
+// lane apart (two of the warp's reads cover 512 contiguous bytes).
+__device__ __forceinline__ int mx_x_index(int v, int i, int lane)
+{
+    return ((v * (kMxPairs / 2) + (i >> 1)) * 32 + lane) * 2 + (i & 1);
+}
+
+// Stages x[v][k0 .. k0 + kn) for v < V into xs at mx_x_index as fp32 pairs
+// (element 2i of block l in the low half). kn is a multiple of 32. Thread
+// item t of a vector takes the 8 elements (t / 32) * 8 .. + 7 of block t % 32,
+// so the 32 threads of a warp write the same pair of 32 consecutive lanes.
 template <int V>
 __device__ __forceinline__ void mx_stage_chunk(uint64_t *xs, const uint16_t *x, int K, int k0, int kn)
 {
@@ -119,11 +127,10 @@ __device__ __forceinline__ void mx_stage_chunk(uint64_t *xs, const uint16_t *x, 
         const int e0 = blk * 32 + quad * 8;
         if (e0 >= kn) continue;
         const uint4 u = __ldg(reinterpret_cast<const uint4 *>(x + size_t(v) * K + k0 + e0));
-        uint64_t *dst = xs + (size_t(v) * kMxPairs + quad * 4) * 32 + blk;
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-            dst[q * 32] = (uint64_t(w[q] & 0xffff0000u) << 32) | uint64_t(w[q] << 16);
+            xs[mx_x_index(v, quad * 4 + q, blk)] = (uint64_t(w[q] & 0xffff0000u) << 32) | uint64_t(w[q] << 16);
     }
 }
 
@@ -193,7 +200,7 @@ __device__ __forceinline__ void mx_pass(const MxParams &p, uint64_t *xs, int v0,
                     for (int r = 0; r < kMxRows; ++r) wv[r] = f16x2_to_f32x2(h[r][k]);
 #pragma unroll
                     for (int v = 0; v < VPN; ++v) {
-                        const uint64_t x2 = xs[(v * kMxPairs + i) * 32 + lane];
+                        const uint64_t x2 = xs[mx_x_index(v, i, lane)];
 #pragma unroll
                         for (int r = 0; r < kMxRows; ++r) acc[v][r] = mx_ffma2(wv[r], x2, acc[v][r]);
                     }
@@ -251,7 +258,7 @@ template <int V>
 __global__ void __launch_bounds__(kMxWarps * 32, mx_min_blocks<V>()) qmv_mxfp4(MxParams p)
 {
     if constexpr (V >= 5) {
-        extern __shared__ __align__(16) uint64_t mx_xs[];  // [VP][kMxPairs][32] fp32 pairs
+        extern __shared__ __align__(16) uint64_t mx_xs[];  // VP vectors of staged x (mx_x_index)
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
         const int row0 = blockIdx.x * kMxRowsPerCta + warp * kMxRows;
         const int nlive = p.N - row0;
@@ -268,7 +275,7 @@ __global__ void __launch_bounds__(kMxWarps * 32, mx_min_blocks<V>()) qmv_mxfp4(M
 template <int V>
 __device__ __forceinline__ void qmv_mxfp4_narrow(MxParams p)
 {
-    extern __shared__ __align__(16) uint64_t mx_xs[];  // [V][kMxPairs][32] fp32 pairs
+    extern __shared__ __align__(16) uint64_t mx_xs[];  // V vectors of staged x (mx_x_index)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int row0 = blockIdx.x * kMxRowsPerCta + warp * kMxRows;
     const int B = p.K >> 5;  // scale blocks per row
@@ -343,7 +350,7 @@ __device__ __forceinline__ void qmv_mxfp4_narrow(MxParams p)
 #pragma unroll
                         for (int v = 0; v < kMxPass; ++v) {
                             if (v0 + v >= V) continue;
-                            const uint64_t xv = mx_xs[((v0 + v) * kMxPairs + i) * 32 + lane];
+                            const uint64_t xv = mx_xs[mx_x_index(v0 + v, i, lane)];
 #pragma unroll
                             for (int r = 0; r < kMxRows; ++r) acc[v][r] = mx_ffma2(wv[r], xv, acc[v][r]);
                         }
