@@ -28,7 +28,7 @@
 // sm_100-class parts (two elements per instruction, exact) and one exact
 // f16 -> f32 widening each; the two chains run as one packed fma.rn.f32x2.
 //
-// A CTA holds 8 warps of 4 rows each. K goes by in chunks of 1024 elements,
+// A CTA holds 4 warps of 4 rows each. K goes by in chunks of 1024 elements,
 // one 32-block per lane; each chunk of x is staged once per CTA into shared
 // memory as fp32 pairs laid out [vector][pair / 2][lane][pair % 2] (a warp's
 // reads of two pairs cover 512 contiguous bytes), and every x pair read serves the
@@ -37,8 +37,10 @@
 // next chunk's weights are loaded while the current one is computed. From 5
 // vectors on, the vectors go in passes of at most 5 outermost, each over all
 // of K with its partials in registers (mx_pass), so a chunk's weights convert
-// once per pass and a CTA needs at most 20 KB of shared memory: two CTAs (16
-// warps) share an SM.
+// once per pass and a CTA needs at most 20 KB of shared memory: four CTAs (16
+// warps) share an SM. 16 rows a CTA keep the last wave short: a 15360-row
+// matrix is 960 CTAs, 6.3 per SM (with 32 rows a CTA, 3.2 per SM, the last
+// of them ran on a half-empty GPU).
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -51,9 +53,9 @@
 namespace qmv {
 namespace {
 
-constexpr int kMxWarps = 8;
+constexpr int kMxWarps = 4;
 constexpr int kMxRows = 4;                         // rows per warp
-constexpr int kMxRowsPerCta = kMxWarps * kMxRows;  // 32
+constexpr int kMxRowsPerCta = kMxWarps * kMxRows;  // 16
 constexpr int kMxChunk = 32 * 32;                  // elements per K-chunk: one 32-block per lane
 constexpr int kMxPairs = 16;                       // element pairs per block
 constexpr int kMxPass = 4;                         // vectors per pass over a chunk's weights
@@ -134,11 +136,11 @@ __device__ __forceinline__ void mx_stage_chunk(uint64_t *xs, const uint16_t *x, 
     }
 }
 
-// CTAs per SM the register budget must allow: four for one vector (at most
-// 64 registers), so that a 15360-row matrix (480 CTAs) runs as one wave on
-// 152 SMs; two otherwise (at most 128 registers).
+// CTAs per SM the register budget must allow: eight for one vector (at most
+// 64 registers), so that a 15360-row matrix (960 CTAs) runs as one wave on
+// 152 SMs; four otherwise (at most 128 registers, 16 warps per SM).
 template <int V>
-constexpr int mx_min_blocks() { return V == 1 ? 4 : 2; }
+constexpr int mx_min_blocks() { return V == 1 ? 8 : 4; }
 
 // Several vectors (V >= 5): the vectors go in passes of at most kMxWidePass,
 // each pass running over all of K, so that a pass's partials stay in
@@ -302,7 +304,7 @@ __device__ __forceinline__ void qmv_mxfp4_narrow(MxParams p)
         }
     };
     // Several vectors: the next chunk's loads are issued a chunk ahead. One
-    // vector: a chunk's loads are issued before its x is staged; the four CTAs
+    // vector: a chunk's loads are issued before its x is staged; the eight CTAs
     // an SM then holds keep enough of them in flight, and the 64-register
     // budget has no room for a second set.
     constexpr bool kAhead = V > 1;
