@@ -528,6 +528,14 @@ struct Traits {
     static constexpr int NVAL = kRows * VP;
     static constexpr int NRED = NVAL <= 4 ? 4 : NVAL <= 8 ? 8 : NVAL <= 16 ? 16 : 32;
     static constexpr int NP = BITS == 4 ? 2 : 1;              // 16-byte pieces per subgroup row
+    // Two equal passes of at least 7 vectors (V = 14, 16): each pass of a unit
+    // is a work item of its own (both load the unit's weights), so a CTA's
+    // last items spread over more warps (V = 16: 6 % faster). Otherwise a
+    // unit's passes form one item, its weights parked in shared memory
+    // between them (splitting them measured 1-6 % slower there).
+    static constexpr bool SPLIT = PASSES == 2 && 2 * VP == V && VP >= 7;
+    static constexpr int IPU = SPLIT ? PASSES : 1;  // work items per unit
+    static constexpr int PPI = SPLIT ? 1 : PASSES;  // passes per work item
 };
 
 // Steps 1 and 2 for eight consecutive elements of a subgroup, held as raw
@@ -1297,7 +1305,7 @@ __device__ __forceinline__ void qmv_direct_body(const Params &p)
 
     uint32_t poff[T::NP];
     piece_offsets<BITS>(lane, poff);
-    // The next unit for this warp (units are taken in increasing order).
+    // The next work item for this warp (items are taken in increasing order).
     auto grab = [&]() {
         int u = 0;
         if (lane == 0) u = int(atomicAdd(s_next, 1u));
@@ -1342,12 +1350,14 @@ __device__ __forceinline__ void qmv_direct_body(const Params &p)
         }
     };
 
-    // The first unit's loads first: they do not depend on the preceding grid
-    // (the call's staging kernel), so their latency overlaps it.
-    int u0 = grab();
+    // The first item's loads first: they do not depend on the preceding grid
+    // (the call's staging kernel), so their latency overlaps it. Item i is
+    // unit i / IPU, passes from (i % IPU) * PPI on.
+    const int nitems = nunits * T::IPU;
+    int i0 = grab();
     uint4 w_cur[kRows][T::NP];
     uint32_t s_cur[kRows] = {0, 0, 0, 0}, b_cur[kRows] = {0, 0, 0, 0};
-    if (u0 < nunits) load_unit(u0, w_cur, s_cur, b_cur);
+    if (i0 < nitems) load_unit(i0 / T::IPU, w_cur, s_cur, b_cur);
     grid_launch_dependents();
     grid_dependency_wait();  // the staged cells are written by the preceding grid
     constexpr uint32_t kCell = kXsF32;
@@ -1369,7 +1379,8 @@ __device__ __forceinline__ void qmv_direct_body(const Params &p)
 
     const uint32_t xv_bytes = uint32_t(nsub_max) * kXsF32;
     const uint32_t wcell = smem_u32(smem + L.wbuf) + uint32_t(warp) * kRows * T::NP * 512u + uint32_t(lane) * 16u;
-    while (u0 < nunits) {
+    while (i0 < nitems) {
+        const int u0 = i0 / T::IPU, ps0 = (i0 - u0 * T::IPU) * T::PPI;
         const Unit g = unit_geo(u0);
         const bool active = g.t < p.S_row;
         const int sl = (active ? g.t : g.cc * kChunkSubs) - sub_lo;  // a staged subgroup for idle lanes
@@ -1379,20 +1390,20 @@ __device__ __forceinline__ void qmv_direct_body(const Params &p)
             fs[r] = bf16_bits_to_f32(s_cur[r]);
             fb[r] = bf16_bits_to_f32(b_cur[r]);
         }
-        // two passes: park the weight bytes in this lane's cells of the
-        // warp's buffer (only this lane reads them back)
-        if constexpr (T::PASSES > 1) {
+        // two passes in this item: park the weight bytes in this lane's cells
+        // of the warp's buffer (only this lane reads them back)
+        if constexpr (T::PPI > 1) {
 #pragma unroll
             for (int r = 0; r < kRows; ++r)
 #pragma unroll
                 for (int pc = 0; pc < T::NP; ++pc) sts_v4_u32(wcell + uint32_t(r * T::NP + pc) * 512u, w_cur[r][pc]);
         }
 #pragma unroll
-        for (int ps = 0; ps < T::PASSES; ++ps) {
-            const int v0 = ps * T::VP;
+        for (int pp = 0; pp < T::PPI; ++pp) {
+            const int v0 = (ps0 + pp) * T::VP;
             const uint32_t xsub = xs + (uint32_t(v0) * nsub_max + sl) * kXsF32;
             uint64_t acc[kRows][T::VP];
-            if constexpr (T::PASSES > 1)
+            if constexpr (T::PPI > 1)
                 subgroup_dot_vp_smem<BITS, T::VP>(wcell, xsub, xv_bytes, acc);
             else
                 subgroup_dot_vp<BITS, T::VP>(w_cur, xsub, xv_bytes, acc);
@@ -1417,10 +1428,10 @@ __device__ __forceinline__ void qmv_direct_body(const Params &p)
             if ((lane & ((1 << SH) - 1)) == 0 && idx < T::NVAL && v0 + v < V && r < g.nr)
                 cvs[((g.r0 - row_t0 + r) * cpc_here + (g.cc - c_lo)) * V + v0 + v] = tot;
         }
-        // the next unit: its loads are issued only now (the other warps'
+        // the next item: its loads are issued only now (the other warps'
         // arithmetic covers their latency)
-        u0 = grab();
-        if (u0 < nunits) load_unit(u0, w_cur, s_cur, b_cur);
+        i0 = grab();
+        if (i0 < nitems) load_unit(i0 / T::IPU, w_cur, s_cur, b_cur);
     }
     __syncthreads();
     fold_chunks<V>(cvs, (rb_hi - rb_lo) * kRows, row_t0, c_lo, cpc_here, rb_lo, tid, nthreads, p.N, p.ks, p.cpc,
