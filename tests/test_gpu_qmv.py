@@ -43,6 +43,7 @@ MEDIUM = [
     (200, 3840, 3, 4, 64),      # K of the 12B projection: 2 chunks, 7.5 stages
     (130, 15360, 2, 4, 64),     # K of the down projection: 8 chunks
     (77, 5120, 16, 4, 64),      # widest M
+    (90, 3840, 14, 4, 64),      # two passes, each its own work item
     (300, 3840, 13, 2, 64),
     (150, 3840, 5, 2, 128),
     (129, 2048, 4, 4, 128),
@@ -102,7 +103,9 @@ def test_streamed_columns_bit_identical_to_m1(N, K, bits, gs):
     dp = DeviceProblem(inp)
     singles_bf = np.stack([dp.run(x=dp.x[m:m + 1].contiguous(), M=1)[0] for m in range(16)])
     singles_32 = np.stack([dp.run(x=dp.x[m:m + 1].contiguous(), M=1, flags=g.F32_OUT)[0] for m in range(16)])
-    for M in (2, 4, 5, 10, 13, 16):
+    # every pass structure: one pass (2..8), two unequal (9, 13), two equal in
+    # one work item (10), two equal passes as separate work items (14, 16)
+    for M in (2, 4, 5, 9, 10, 13, 14, 16):
         x = dp.x[:M].contiguous()
         y_bf = dp.run(x=x, M=M)
         y_32 = dp.run(x=x, M=M, flags=g.F32_OUT)
