@@ -1,11 +1,9 @@
 // qmv_run_noalloc: the mat-vec without any device allocation.
 //
-// Some callers cannot call cudaMalloc: code that runs while a CUDA graph is
-// being captured (an allocation there is not stream-ordered and breaks or
-// serializes the capture), engines whose device memory all belongs to their
-// own pool allocator (a private cudaMalloc fragments it and can fail under
-// memory pressure), and latency-bound decode loops (cudaMalloc may
-// synchronize the whole device). qmv_run allocates its workspace on first
+// Some callers cannot call cudaMalloc: engines whose device memory all
+// belongs to their own pool allocator (a private cudaMalloc fragments it and
+// can fail under memory pressure), and latency-bound decode loops (cudaMalloc
+// may synchronize the whole device). qmv_run allocates its workspace on first
 // use, and qmv_run_ex needs a workspace the caller allocated; this entry point
 // needs neither. The scratch that K-split launches use lives in one
 // fixed-size array of this file instead.

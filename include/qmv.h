@@ -198,13 +198,11 @@ QMV_API qmv_status qmv_run_ex(const uint32_t *w_q, const uint16_t *scales, const
 #define QMV_NOALLOC_SCRATCH_BYTES (8u << 20)
 
 /* qmv_run without any device allocation. The paper has no counterpart: this
- * entry point exists for callers that cannot call cudaMalloc -- code running
- * during CUDA graph capture (an allocation is not stream-ordered and breaks
- * or serializes the capture), engines whose device memory all belongs to
- * their own pool allocator, and latency-bound decode loops where cudaMalloc's
- * implicit device synchronization is not acceptable. qmv_run allocates its
- * workspace on first use and qmv_run_ex needs a caller-allocated one; this
- * call needs neither.
+ * entry point exists for callers that cannot call cudaMalloc -- engines whose
+ * device memory all belongs to their own pool allocator, and latency-bound
+ * decode loops where cudaMalloc's implicit device synchronization is not
+ * acceptable. qmv_run allocates its workspace on first use and qmv_run_ex
+ * needs a caller-allocated one; this call needs neither.
  *
  * Arguments, layouts, results (bit for bit) and the host-side errors are those
  * of qmv_run. The scratch that K-split problems need comes from one static
@@ -215,8 +213,9 @@ QMV_API qmv_status qmv_run_ex(const uint32_t *w_q, const uint16_t *scales, const
  * race and give undefined results.
  *
  * The first call on a device, whatever its shape, looks up the array's
- * device address (cudaGetSymbolAddress) with that device current; make that
- * first call before any stream capture.
+ * device address (cudaGetSymbolAddress) with that device current, which may
+ * load the library's device code and wait for the device; later calls on that
+ * device make no such lookup.
  *
  * Errors: those of qmv_run, checked first and in the same order; then
  * QMV_ERR_WORKSPACE when the problem's qmv_workspace_size() exceeds

@@ -1,5 +1,5 @@
 """qmv_run_noalloc: the entry point for callers that cannot allocate device
-memory (graph capture, pool-owned memory, latency-bound loops). It must give
+memory (pool-owned memory, latency-bound loops). It must give
 the same output as the existing qmv_run_ex path, call after call, while its
 scratch lives in a fixed array inside the library.
 
