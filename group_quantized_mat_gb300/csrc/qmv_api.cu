@@ -80,6 +80,11 @@ constexpr int kCvBudget = 16 * 1024;
 // One-vector kernel: staged x at most, largest unit, ring depth.
 constexpr int kXsBudgetV1 = 80 * 1024;
 constexpr int kUnitMax = 8 * 1024;
+// Whole-row units may be up to 10 KB (four rows of K = 5120 at 4 bits) when
+// every consumer warp gets at least two of them: a 17408 x 5120 matrix then
+// runs 3 % faster on the ring than on the direct-load kernel, while 5120 x 5120
+// (one unit per consumer) runs 15 % slower.
+constexpr int kUnitMaxRows = 10 * 1024;
 constexpr int kMaxSlots = 32;
 // Rows at least this long go to the ring whatever their unit shape.
 constexpr int kRingMinK = 12288;
@@ -160,7 +165,7 @@ Problem plan_ring(int N, int K, int bits, int gs, int sms, bool sb_packed)
     pr.consumers = qmv::kRingConsumers;
     grid_shape(pr, sms, 1, kCvBudget);
     const int cb = qmv::chunk_bytes(bits);
-    bool whole = pr.cpc == pr.ks && qmv::kRows * pr.row_bytes <= kUnitMax;
+    bool whole = pr.cpc == pr.ks && qmv::kRows * pr.row_bytes <= kUnitMaxRows;
     if (whole) {
         pr.unit_mode = qmv::kUnitRows;
         pr.uc = pr.ks;
@@ -251,6 +256,11 @@ Problem plan(int V, int N, int K, int bits, int gs, int sms, bool sb_packed = fa
     // otherwise the direct-load kernel, whose units need no per-row copies.
     const long long four_rows = (long long)qmv::kRows * K * bits / 8;
     if (four_rows <= kUnitMax || K >= kRingMinK) return plan_ring(N, K, bits, gs, sms, sb_packed);
+    if (four_rows <= kUnitMaxRows) {
+        // whole-row units of up to 10 KB, if each consumer warp gets two
+        const Problem pr = plan_ring(N, K, bits, gs, sms, sb_packed);
+        if (pr.unit_mode == qmv::kUnitRows && (long long)pr.NB >= 2LL * pr.consumers * pr.grid_rows) return pr;
+    }
     return plan_one(N, K, bits, gs, sms, sb_packed);
 }
 

@@ -90,6 +90,17 @@ def test_parity_full_size_all_rows(o, name, M):
     check_parity(y, ref, terms, f"{name} M={M}")
 
 
+# Rows whose four-row unit is 8-10 KB go to the ring (one copy of whole rows)
+# when every consumer warp gets two units, else to the direct-load kernel: both
+# sides of that rule, at 4 and 2 bits, every row against the oracle.
+@pytest.mark.parametrize("N,K,bits,gs", [(9728, 9216, 2, 64), (12288, 5120, 4, 128), (2048, 4608, 4, 64)])
+def test_parity_long_whole_row_units(o, N, K, bits, gs):
+    inp = synth.make_inputs(N, K, 1, bits, gs, seed=N + K)
+    y = DeviceProblem(inp).run()
+    ref, terms = oracle_rows(o, inp)
+    check_parity(y, ref, terms, f"{N}x{K} {bits}-bit g{gs}")
+
+
 # ------------------------------------------------------- bit identity --
 IDENT = [
     (15360, 3840, 4, 64), (3840, 15360, 4, 64), (1000, 5120, 4, 64),
