@@ -134,17 +134,25 @@ Problem plan_direct(int V, int N, int K, int bits, int gs, int sms)
 {
     Problem pr{};
     common_shape(pr, V, N, K, bits, gs);
-    const int warps = qmv::kStreamedWarps;
-    const int wbuf = qmv::vectors_per_pass(V) < V ? warps * qmv::kRows * 32 * qmv::sub_bytes(bits) : 0;
     auto nsub_of = [&](int cpc) { return cpc * qmv::kChunkSubs < pr.S_row ? cpc * qmv::kChunkSubs : pr.S_row; };
     auto xs_bytes = [&](int cpc) { return qmv::align_up(V * nsub_of(cpc) * qmv::kXsF32, 16); };
+    // Two or three vectors whose cells of all of K fit half the shared memory:
+    // CTAs of 8 warps, two per SM (their registers allow it), so more warps
+    // cover each other's weight loads (15360 x 3840 at M = 2: 17.3 -> 15.8 us).
+    // Where that would split K (3840 x 15360), the split cost more than the
+    // warps gained.
+    const int half = kSmemBudget / 2 - 256;
+    const int per_sm = V <= 3 && xs_bytes(pr.ks) + kCvBudget + 16 + 128 <= half ? 2 : 1;
+    const int warps = per_sm == 2 ? 8 : qmv::kStreamedWarps;
+    const int budget = per_sm == 2 ? half : kSmemBudget;
+    const int wbuf = qmv::vectors_per_pass(V) < V ? warps * qmv::kRows * 32 * qmv::sub_bytes(bits) : 0;
     pr.cpc = pr.ks;
-    while (pr.cpc > 1 && xs_bytes(pr.cpc) + kCvBudget + wbuf + 16 + 128 > kSmemBudget) --pr.cpc;
+    while (pr.cpc > 1 && xs_bytes(pr.cpc) + kCvBudget + wbuf + 16 + 128 > budget) --pr.cpc;
     pr.cpc = balanced_cpc(pr.ks, pr.cpc);
     pr.threads = 32 * warps;
     // chunk values may use whatever shared memory the x cells and the weight
     // buffer leave (at least kCvBudget, by the fit above)
-    grid_shape(pr, sms, V, kSmemBudget - (xs_bytes(pr.cpc) + wbuf + 16 + 128 + 16));
+    grid_shape(pr, per_sm * sms, V, budget - (xs_bytes(pr.cpc) + wbuf + 16 + 128 + 16));
     pr.smem = qmv::smem_layout(bits, V, warps, nsub_of(pr.cpc), pr.max_rb, pr.cpc).total;
     return pr;
 }

@@ -1438,9 +1438,10 @@ __device__ __forceinline__ void qmv_direct_body(const Params &p)
                    p.partials, p.counters, p.y, p.f32_out);
 }
 
-// Launch bounds: the one-vector kernel runs 16 consumer warps and 4 producer
-// warps; the streamed kernel 12 warps (its registers go to the V-vector
-// accumulators).
+// Launch bounds: the one-vector kernel runs at most 16 consumer warps and 4
+// producer warps; the streamed kernel at most 12 warps (its registers go to
+// the V-vector accumulators; at two or three vectors the plan may launch
+// 8-warp CTAs, two per SM).
 constexpr int kConsumersV1 = 16;
 constexpr int kProducersV1 = 4;
 constexpr int kThreadsV1 = (kConsumersV1 + kProducersV1) * 32;
