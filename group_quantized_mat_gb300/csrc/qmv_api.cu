@@ -69,6 +69,7 @@ struct Problem {
     int smem;       // dynamic shared memory per CTA
     // one-vector ring
     int uc, unit_mode, pitch, sb_mode_unit, sbox, slots, consumers;
+    int ringv;      // 2..4 vectors through the ring (staged cells from the workspace)
     int sb_packed;
 };
 
@@ -163,15 +164,16 @@ Problem plan_direct(int V, int N, int K, int bits, int gs, int sms)
 // are 16-byte multiples, else one copy per row), scale/bias boxes, then as
 // many ring slots as fit (a multiple of the producer warps, at most kMaxSlots
 // and the CTA's units).
-Problem plan_ring(int N, int K, int bits, int gs, int sms, bool sb_packed)
+Problem plan_ring(int N, int K, int bits, int gs, int sms, bool sb_packed, int V = 1)
 {
     Problem pr{};
-    common_shape(pr, 1, N, K, bits, gs);
-    // raw x (128 bytes a subgroup) and its staged cell (kXsB16 bytes)
-    const int per_sub = 128 + qmv::kXsB16;
+    common_shape(pr, V, N, K, bits, gs);
+    // raw x (128 bytes a subgroup) and its staged cell (kXsB16 bytes); V >= 2:
+    // the V staged fp32 cells
+    const int per_sub = V == 1 ? 128 + qmv::kXsB16 : V * qmv::kXsF32;
     pr.cpc = pr.S_row * per_sub <= kXsBudgetV1 ? pr.ks : balanced_cpc(pr.ks, kXsBudgetV1 / (qmv::kChunkSubs * per_sub));
     pr.consumers = qmv::kRingConsumers;
-    grid_shape(pr, sms, 1, kCvBudget);
+    grid_shape(pr, sms, V, kCvBudget);
     const int cb = qmv::chunk_bytes(bits);
     bool whole = pr.cpc == pr.ks && qmv::kRows * pr.row_bytes <= kUnitMaxRows;
     if (whole) {
@@ -206,7 +208,7 @@ Problem plan_ring(int N, int K, int bits, int gs, int sms, bool sb_packed)
     }
     const int nsub = pr.cpc * qmv::kChunkSubs < pr.S_row ? pr.cpc * qmv::kChunkSubs : pr.S_row;
     auto layout = [&](int slots) {
-        return qmv::ring_layout(pr.pitch, pr.sb_mode_unit, pr.sbox, pr.sb_packed, slots, nsub, pr.max_rb, pr.cpc);
+        return qmv::ring_layout(pr.pitch, pr.sb_mode_unit, pr.sbox, pr.sb_packed, slots, nsub, pr.max_rb, pr.cpc, V);
     };
     // Slots: a multiple of the producer and the consumer counts (each slot
     // has one producer and one consumer warp). A consumer warp with a single
@@ -216,13 +218,14 @@ Problem plan_ring(int N, int K, int bits, int gs, int sms, bool sb_packed)
     // not fit).
     const int P = qmv::kRingProducers;
     int C = 0;
+    const int cmax = V == 1 ? qmv::kRingConsumers : 12;
     for (int c : {qmv::kRingConsumers, 12, 8})
-        if (c <= qmv::kRingConsumers && layout(2 * c).total <= kSmemBudget) {
+        if (c <= cmax && layout(2 * c).total <= kSmemBudget) {
             C = c;
             break;
         }
     if (C == 0) {
-        C = qmv::kRingConsumers;
+        C = cmax;
         while (C > P && layout(C).total > kSmemBudget) C /= 2;
     }
     int slots = C;
@@ -258,7 +261,18 @@ Problem plan_one(int N, int K, int bits, int gs, int sms, bool sb_packed)
 
 Problem plan(int V, int N, int K, int bits, int gs, int sms, bool sb_packed = false)
 {
-    if (V >= 2) return plan_direct(V, N, K, bits, gs, sms);
+    if (V >= 2) {
+        // 2..4 vectors over whole-row units: the ring, consumers running the
+        // packed-fma datapath on the call's staged cells
+        if (V <= 4 && (long long)qmv::kRows * K * bits / 8 <= kUnitMax) {
+            Problem pr = plan_ring(N, K, bits, gs, sms, sb_packed, V);
+            if (pr.unit_mode == qmv::kUnitRows && pr.cpc == pr.ks && pr.consumers >= 4) {
+                pr.ringv = 1;
+                return pr;
+            }
+        }
+        return plan_direct(V, N, K, bits, gs, sms);
+    }
     // One vector: the ring when a unit is four whole rows in one copy, or
     // for long rows (where staging x once per SM, not per CTA, matters);
     // otherwise the direct-load kernel, whose units need no per-row copies.
@@ -441,6 +455,19 @@ cudaError_t dispatch(const Problem &pr, const qmv::RingMaps &maps, const qmv::Pa
         // kernel unless QMV_PDL allows the weights to stream under it.
         l.pdl = true;
     }
+    if (pr.ringv) {
+        qmv::RingParams rp;
+        static_cast<qmv::Params &>(rp) = p;
+        rp.uc = pr.uc; rp.unit_mode = pr.unit_mode; rp.pitch = pr.pitch; rp.sb_mode_unit = pr.sb_mode_unit;
+        rp.sbox = pr.sbox; rp.slots = pr.slots; rp.consumers = pr.consumers;
+        // the staging kernel before it writes no weights and started after the
+        // stream's earlier work completed: the weights may stream under it
+        rp.early_weights = 1;
+        if (pr.bits == 4 && pr.gs == 64) return qmv::launch_b4g64_ringv(pr.V, maps, rp, l, stream);
+        if (pr.bits == 4 && pr.gs == 128) return qmv::launch_b4g128_ringv(pr.V, maps, rp, l, stream);
+        if (pr.bits == 2 && pr.gs == 64) return qmv::launch_b2g64_ringv(pr.V, maps, rp, l, stream);
+        return qmv::launch_b2g128_ringv(pr.V, maps, rp, l, stream);
+    }
     if (pr.V == 1 && pr.unit_mode == kUnitOne) {
         if (pr.bits == 4 && pr.gs == 64) return qmv::launch_b4g64_one(p, l, stream);
         if (pr.bits == 4 && pr.gs == 128) return qmv::launch_b4g128_one(p, l, stream);
@@ -547,7 +574,7 @@ qmv_status run_impl(const uint32_t *w_q, const uint16_t *scales, const uint16_t 
 
         qmv::RingMaps maps;
         memset(&maps, 0, sizeof maps);
-        if (V == 1 && pr.unit_mode != kUnitOne) {
+        if ((V == 1 && pr.unit_mode != kUnitOne) || pr.ringv) {
             int enc = encode_sb_map(&maps.s, scales, pr);
             if (enc == 0 && !sb_packed) enc = encode_sb_map(&maps.b, biases, pr);
             if (enc == 0 && pr.unit_mode == qmv::kUnitTiles) enc = encode_w_map(&maps.w, w_q, pr);

@@ -19,4 +19,8 @@ cudaError_t launch_b2g128_stage(const uint16_t *x, int K, int S_row, int V, uint
 {
     return launch_stage<2>(x, K, S_row, V, out, counters, ncounters, pdl, stream);
 }
+cudaError_t launch_b2g128_ringv(int V, const RingMaps &maps, const RingParams &p, const Launch &l, cudaStream_t stream)
+{
+    return launch_ringv<2, 128>(V, maps, p, l, stream);
+}
 }  // namespace qmv

@@ -789,7 +789,7 @@ __device__ __forceinline__ void fold_chunks(const float *cvs, int nrows, int row
 
 // ------------------------------------------------------- one vector: ring --
 
-template <int BITS, int GS, bool SBP>
+template <int BITS, int GS, bool SBP, int V = 1>
 __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CUtensorMap *map_s, const CUtensorMap *map_b,
                                               const RingParams &p)
 {
@@ -818,7 +818,7 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CU
     const int nunits = (rb_hi - rb_lo) * upr;
 
     const int nsub_max = p.cpc * kChunkSubs < p.S_row ? p.cpc * kChunkSubs : p.S_row;
-    const RingLayout L = ring_layout(p.pitch, p.sb_mode_unit, p.sbox, SBP, p.slots, nsub_max, p.max_rb, p.cpc);
+    const RingLayout L = ring_layout(p.pitch, p.sb_mode_unit, p.sbox, SBP, p.slots, nsub_max, p.max_rb, p.cpc, V);
     // metadata: bytes per element (a bf16, or an interleaved scale|bias pair)
     // and the box start alignment in elements (16 bytes)
     constexpr int sbE = sb_elem_bytes(SBP), sbA = 16 / sbE;
@@ -955,16 +955,26 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CU
         // alone: the producer refills a slot only after its one consumer has
         // released the unit before.
         grid_dependency_wait();  // x may be written by the preceding grid
-        if (tid == 0) {
-            // the CTA's x range in one copy, landing where it is staged from
-            mbar_arrive_expect_tx(xbar, uint32_t(nsub) * 128u);
-            bulk_load_plain(xr, p.x + size_t(sub_lo) * kSub, uint32_t(nsub) * 128u, xbar);
+        if constexpr (V == 1) {
+            if (tid == 0) {
+                // the CTA's x range in one copy, landing where it is staged from
+                mbar_arrive_expect_tx(xbar, uint32_t(nsub) * 128u);
+                bulk_load_plain(xr, p.x + size_t(sub_lo) * kSub, uint32_t(nsub) * 128u, xbar);
+            }
+        } else {
+            if (tid == 0) {
+                // the call's staged cells of this CTA's range, one copy per vector
+                mbar_arrive_expect_tx(xbar, uint32_t(V * nsub) * kXsF32);
+                for (int v = 0; v < V; ++v)
+                    bulk_load_plain(xc + uint32_t(v * nsub) * kXsF32, p.xs_staged + (size_t(v) * p.S_row + sub_lo) * kXsF32,
+                                    uint32_t(nsub) * kXsF32, xbar);
+            }
         }
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(xbar, 0)) && lane == 0) {
             atomicOr(p.err, 1u);
             *s_abort = 1;
         }
-        stage_x_cells<BITS>(xr, xc, sub_lo, nsub, tid, C * 32);
+        if constexpr (V == 1) stage_x_cells<BITS>(xr, xc, sub_lo, nsub, tid, C * 32);
         asm volatile("bar.sync 1, %0;" ::"r"(C * 32) : "memory");  // consumer warps only
 
         uint32_t poff[NP];
@@ -1032,10 +1042,38 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CU
                         fb[r] = bf16_bits_to_f32(lds_u16(ba[r] + go));
                     }
                 }
-                const uint32_t cell = xc + uint32_t(tl - sub_lo) * uint32_t(kXsB16);
-                const float tot = chunk_v1<BITS, false>(quads, cell, 0u, cell + 128u, fs, fb, active, lane);
-                const int r = lane >> 3;
-                if ((lane & 7) == 0 && r < g.nr) cvs[(g.r0 - row_t0 + r) * cpc_here + (cc - c_lo)] = tot;
+                if constexpr (V == 1) {
+                    const uint32_t cell = xc + uint32_t(tl - sub_lo) * uint32_t(kXsB16);
+                    const float tot = chunk_v1<BITS, false>(quads, cell, 0u, cell + 128u, fs, fb, active, lane);
+                    const int r = lane >> 3;
+                    if ((lane & 7) == 0 && r < g.nr) cvs[(g.r0 - row_t0 + r) * cpc_here + (cc - c_lo)] = tot;
+                } else {
+                    // V vectors: fp32 cells, packed fmas (the streamed kernel's datapath)
+                    constexpr int NVAL = kRows * V;
+                    constexpr int NRED = NVAL <= 4 ? 4 : NVAL <= 8 ? 8 : NVAL <= 16 ? 16 : 32;
+                    const uint32_t xv_bytes = uint32_t(nsub) * kXsF32;
+                    const uint32_t xsub = xc + uint32_t(tl - sub_lo) * kXsF32;
+                    uint64_t acc[kRows][V];
+                    subgroup_dot_vp<BITS, V>(quads, xsub, xv_bytes, acc);
+                    float val[NRED];
+#pragma unroll
+                    for (int i = 0; i < NRED; ++i) val[i] = 0.0f;
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        const float4 meta = lds_f4(xsub + v * xv_bytes + 256);
+#pragma unroll
+                        for (int r = 0; r < kRows; ++r) {
+                            const float term = subgroup_term<true>(pair_lo(acc[r][v]), pair_hi(acc[r][v]), fs[r], fb[r], meta.x, meta.y, meta.z);
+                            val[r * V + v] = active ? term : 0.0f;
+                        }
+                    }
+                    const float tot = tree_reduce_scatter<NRED>(val, lane);
+                    constexpr int SH = NRED == 4 ? 3 : NRED == 8 ? 2 : NRED == 16 ? 1 : 0;
+                    const int idx = lane >> SH;
+                    const int r = idx / V, v = idx - r * V;
+                    if ((lane & ((1 << SH) - 1)) == 0 && idx < NVAL && r < g.nr)
+                        cvs[((g.r0 - row_t0 + r) * cpc_here + (cc - c_lo)) * V + v] = tot;
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * slot);
@@ -1059,7 +1097,7 @@ __device__ __forceinline__ void qmv_ring_body(const CUtensorMap *map_w, const CU
         __syncthreads();
         return;
     }
-    fold_chunks<1>(cvs, (rb_hi - rb_lo) * kRows, row_t0, c_lo, cpc_here, rb_lo, tid, nthreads, p.N, p.ks, p.cpc,
+    fold_chunks<V>(cvs, (rb_hi - rb_lo) * kRows, row_t0, c_lo, cpc_here, rb_lo, tid, nthreads, p.N, p.ks, p.cpc,
                    p.partials, p.counters, p.y, p.f32_out);
 }
 
@@ -1454,6 +1492,17 @@ __global__ void __launch_bounds__(kThreadsV1, 1)
            const __grid_constant__ CUtensorMap map_b, const RingParams p)
 {
     qmv_ring_body<BITS, GS, SBP>(&map_w, &map_s, &map_b, p);
+}
+
+// The ring for 2..4 vectors (staged cells from the workspace): at most 12
+// consumer warps and 4 producers, 128 registers.
+constexpr int kThreadsRingV = 16 * 32;
+template <int BITS, int GS, bool SBP, int V>
+__global__ void __launch_bounds__(kThreadsRingV, 1)
+    qmv_ringv(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_s,
+              const __grid_constant__ CUtensorMap map_b, const RingParams p)
+{
+    qmv_ring_body<BITS, GS, SBP, V>(&map_w, &map_s, &map_b, p);
 }
 
 // The one-vector kernel: kOneWarps warps, kOneCtasPerSm CTAs per SM.

@@ -58,6 +58,24 @@ cudaError_t launch_m1(const RingMaps &maps, const RingParams &p, const Launch &l
     return launch_one(qmv_m1<BITS, GS, false>, configured[0], l, stream, maps.w, maps.s, maps.b, p);
 }
 
+template <int BITS, int GS, int V>
+cudaError_t launch_ringv_v(const RingMaps &maps, const RingParams &p, const Launch &l, cudaStream_t stream)
+{
+    static std::atomic<int> configured[2][64] = {};
+    if (p.sb_packed)
+        return launch_one(qmv_ringv<BITS, GS, true, V>, configured[1], l, stream, maps.w, maps.s, maps.b, p);
+    return launch_one(qmv_ringv<BITS, GS, false, V>, configured[0], l, stream, maps.w, maps.s, maps.b, p);
+}
+
+template <int BITS, int GS>
+cudaError_t launch_ringv(int V, const RingMaps &maps, const RingParams &p, const Launch &l, cudaStream_t stream)
+{
+    if (V == 2) return launch_ringv_v<BITS, GS, 2>(maps, p, l, stream);
+    if (V == 3) return launch_ringv_v<BITS, GS, 3>(maps, p, l, stream);
+    if (V == 4) return launch_ringv_v<BITS, GS, 4>(maps, p, l, stream);
+    return cudaErrorInvalidValue;
+}
+
 template <int BITS, int GS>
 cudaError_t launch_one_vector(const Params &p, const Launch &l, cudaStream_t stream)
 {

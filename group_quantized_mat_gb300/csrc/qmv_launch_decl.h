@@ -53,6 +53,7 @@ cudaError_t launch_mxfp4(int V, const MxParams &p, cudaStream_t stream);
 #define QMV_DECLARE_LAUNCH(name)                                                                                  \
     cudaError_t name##_m1(const RingMaps &maps, const RingParams &p, const Launch &l, cudaStream_t stream);      \
     cudaError_t name##_one(const Params &p, const Launch &l, cudaStream_t stream);                               \
+    cudaError_t name##_ringv(int V, const RingMaps &maps, const RingParams &p, const Launch &l, cudaStream_t stream); \
     cudaError_t name##_streamed(int V, const Params &p, const Launch &l, cudaStream_t stream);                   \
     cudaError_t name##_stage(const uint16_t *x, int K, int S_row, int V, uint8_t *out, unsigned *counters,       \
                              int ncounters, bool pdl, cudaStream_t stream);

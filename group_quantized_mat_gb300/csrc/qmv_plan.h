@@ -127,7 +127,7 @@ struct RingLayout {
 __host__ __device__ constexpr int sb_elem_bytes(int sb_packed) { return sb_packed ? 4 : 2; }
 
 __host__ __device__ inline RingLayout ring_layout(int pitch, int sb_mode_unit, int sbox, int sb_packed, int slots,
-                                                  int nsub, int max_rb, int cpc)
+                                                  int nsub, int max_rb, int cpc, int V = 1)
 {
     RingLayout L;
     L.sbs = align_up(sbox * sb_elem_bytes(sb_packed), kBoxAlign);
@@ -136,9 +136,9 @@ __host__ __device__ inline RingLayout ring_layout(int pitch, int sb_mode_unit, i
     L.slot_bytes = L.sb_off + (sb_mode_unit ? 1 : kRows) * (sb_packed ? 1 : 2) * L.sbs;
     L.ring = 0;
     L.xr = slots * L.slot_bytes;
-    L.xc = L.xr + nsub * 128;
-    L.cv = align_up(L.xc + nsub * kXsB16, 16);
-    L.bar = align_up(L.cv + max_rb * kRows * cpc * 4, 16);
+    L.xc = L.xr + (V == 1 ? nsub * 128 : 0);
+    L.cv = align_up(L.xc + (V == 1 ? nsub * kXsB16 : V * nsub * kXsF32), 16);
+    L.bar = align_up(L.cv + max_rb * kRows * cpc * V * 4, 16);
     L.misc = L.bar + (2 * slots + 1) * 8;
     L.total = L.misc + 32 + kBoxAlign;  // next-unit counter, abort flag, issued counts; alignment slack
     return L;
